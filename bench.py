@@ -1,0 +1,509 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 Entropy-Bounded (EB) sampler step of DiffusionGemma.
+
+One step = the whole hot path over one canvas batch: temperature shaping, per-position
+softmax entropy / argmax / Gumbel-max sample over the full vocabulary, entropy-bounded
+selection, re-mask and stop test (DiffusionGemma model card, "Best practices" section 1).
+Workload: B=1 canvas, L=256 positions, V=262144 bf16 logits = 2.5 N(0,1) plus a U(0,12)
+peak per position, 128 of 256 positions masked, T=0.8; ten seeded logit buffers (seeds
+0..9, 10 x 128 MiB > the 126 MB L2) are rotated, and every step starts from a fresh copy
+of its canvas state so each step does the same work.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs its own replica
+(the sampler has no cross-canvas exchange) and the value is all ranks' steps over the
+slowest rank's time.  ``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "EB-sampler steps/s at B×256×262144 bf16; achieved HBM GB/s vs B300 peak"
+B, L, V = 1, 256, 262144
+NSEEDS = 10
+BYTES_PER_STEP = B * L * V * 2           # algorithmic bytes: every logit read once
+TEMPERATURE = 0.8
+WORKLOAD = ("single EB sampler step: B=1 canvas, L=256 positions, V=262144 bf16 logits "
+            "(2.5*N(0,1) + U(0,12) peak per position), 128 of 256 masked, T=0.8")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k1_rowstats_bf16_single_step.md")
+KERNEL_SRC = os.path.join(ROOT, "canvas_sampler_step_b300", "csrc", "eb_sampler.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Maximum of a per-rank scalar (timing) over all ranks."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=f"cuda:{device}" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(steps_per_rank: int, elapsed_s: float, world: int, dist=None, device=None):
+    """(whole-job steps/s, slowest rank's seconds): steps of all ranks / max time."""
+    slowest = max_over_ranks(dist, elapsed_s, device)
+    return steps_per_rank * world / slowest, slowest
+
+
+# ------------------------------------------------------------------ peaks, traffic, clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the row-statistics kernel from the committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("-* `")] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != src_hash:
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self.period = period_s
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self._nv = None
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append((mhz, reasons))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = statistics.median(s[0] for s in self.samples)
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [k for k, v in self.REASONS.items() if bits & v and k != "gpu_idle"]
+        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ the workload
+
+def workload_masks():
+    import eb_synth
+    return np.stack([eb_synth.cfg1_mask(seed)[0] for seed in range(NSEEDS)])
+
+
+def state_pool(n: int, masks: np.ndarray, device):
+    """n fresh canvas states; state i belongs to logits buffer i % NSEEDS."""
+    import torch
+    idx = np.arange(n) % NSEEDS
+    m = torch.from_numpy(masks[idx]).to(device)
+    pool = {
+        "mask": m,
+        "tokens": torch.where(m.bool(), -1, 0).to(torch.int32),
+        "prev_argmax": torch.full((n, L), -1, dtype=torch.int32, device=device),
+        "status": torch.zeros(n, dtype=torch.int32, device=device),
+        "steps_taken": torch.zeros(n, dtype=torch.int32, device=device),
+        "entropy": torch.zeros((n, L), dtype=torch.float32, device=device),
+        "argmax": torch.zeros((n, L), dtype=torch.int32, device=device),
+        "sampled": torch.zeros((n, L), dtype=torch.int32, device=device),
+        "selected": torch.zeros((n, L), dtype=torch.uint8, device=device),
+        "committed": torch.zeros(n, dtype=torch.int32, device=device),
+        "mean_entropy": torch.zeros(n, dtype=torch.float32, device=device),
+    }
+    return pool
+
+
+_ORDER = ("mask", "tokens", "prev_argmax", "status", "steps_taken", "entropy", "argmax",
+          "sampled", "selected", "committed", "mean_entropy")
+
+
+def state_ptrs(pool, i):
+    out = []
+    for k in _ORDER:
+        t = pool[k]
+        row = t[i] if t.dim() > 1 else t[i:i + 1]
+        out.append(row.data_ptr())
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import ctypes
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth
+    import eb_synth.device as synth_dev
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    eb.lib()
+    synth_dev.lib()
+    lib = eb.lib()
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+
+    # inputs resident in HBM before the timed region
+    bufs = []
+    for seed in range(NSEEDS):
+        x = torch.empty((B, L, V), dtype=torch.int16, device=device)
+        synth_dev.logits(synth_dev.Recipe.of(eb_synth.cfg1(seed)), 0, x)
+        bufs.append(x)
+    masks = workload_masks()
+    K, W = args.steps, args.warmup
+    pool = state_pool(W + K, masks, device)
+    ptrs = [state_ptrs(pool, i) for i in range(W + K)]
+    ws_bytes = eb.eb_workspace_bytes(B, L, V, eb.EB_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    params = eb.eb_default_params(seed=0)
+    pref = ctypes.byref(params)
+    buf_ptrs = [b.data_ptr() for b in bufs]
+    wsp = ws.data_ptr()
+    step_fn = lib.eb_sampler_step
+
+    def one(i):
+        st = step_fn(pref, B, L, V, eb.EB_BF16, buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *ptrs[i],
+                     wsp, ws_bytes, sp)
+        if st != 0:
+            raise eb.EbError(st, lib.eb_last_error().decode())
+
+    for i in range(W):
+        one(i)
+    torch.cuda.synchronize()
+
+    k1b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k1e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in k1b + k1e:
+        e.record(stream)          # materialise the CUDA events before timing
+    torch.cuda.synchronize()
+    evb = [e.cuda_event for e in k1b]
+    eve = [e.cuda_event for e in k1e]
+    set_prof = lib.eb_set_profile_events
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for j in range(K):
+            set_prof(evb[j], eve[j])
+            one(W + j)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, local)
+    elapsed = start.elapsed_time(end) / 1e3
+    k1_ms = [b.elapsed_time(e) for b, e in zip(k1b, k1e)]
+    value, slowest = aggregate(K, elapsed, world, dist, local)
+
+    # every timed step did the workload's work: running canvas, one position committed
+    st = pool["status"][W:].cpu().numpy()
+    com = pool["committed"][W:].cpu().numpy()
+    if not ((st == 0).all() and (com >= 1).all()):
+        raise RuntimeError("timed steps did not run the expected workload")
+
+    k1_avg_s = statistics.mean(k1_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = BYTES_PER_STEP / k1_avg_s / 1e9
+    traffic = recorded_traffic()
+
+    e2e = run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world)
+
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": slowest * 1e3 / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded Philox / Box-Muller logits, eb_synth)",
+        "config": {
+            "workload": WORKLOAD,
+            "B": B, "L": L, "V": V, "logits_dtype": "bf16", "masked": 128, "temperature": TEMPERATURE,
+            "l2": "10 rotating 128 MiB logit buffers (1.25 GiB > 126 MB L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm_gbs_step": BYTES_PER_STEP * K / elapsed / 1e9,
+        "positions_per_s": value * B * L,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "k1_rowstats<bf16>",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "k1_ms_mean": statistics.mean(k1_ms),
+            "k1_ms_median": statistics.median(k1_ms),
+            "bytes_per_launch": BYTES_PER_STEP,
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world):
+    """Same steps through the C ABI with host buffers: per step the pinned-host logits
+    and canvas state go to the device, the step runs, its results come back."""
+    import ctypes
+
+    import torch
+    n = max(1, min(args.e2e_steps, args.steps))
+    host_logits = [b.cpu().pin_memory() for b in bufs]
+    dev_logits = torch.empty_like(bufs[0])
+    in_keys = ("mask", "tokens", "prev_argmax", "status")
+    hpool = state_pool(NSEEDS, masks, "cpu")
+    hstate = [{k: hpool[k][s:s + 1].clone().pin_memory() for k in in_keys} for s in range(NSEEDS)]
+    dstate = state_pool(1, masks, device)
+    ptrs = state_ptrs(dstate, 0)
+    out_keys = ("tokens", "mask", "status", "entropy", "argmax", "sampled", "selected")
+    hout = {k: torch.empty_like(dstate[k], device="cpu").pin_memory() for k in out_keys}
+    ws_bytes = eb.eb_workspace_bytes(B, L, V, eb.EB_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    pref = ctypes.byref(params)
+    sp = stream.cuda_stream
+    h2d = host_logits[0].numel() * 2 + sum(
+        hstate[0][k].numel() * hstate[0][k].element_size() for k in in_keys)
+    d2h = sum(hout[k].numel() * hout[k].element_size() for k in out_keys)
+
+    def one(i):
+        s = i % NSEEDS
+        dev_logits.copy_(host_logits[s], non_blocking=True)
+        for k in in_keys:
+            dstate[k].copy_(hstate[s][k], non_blocking=True)
+        st = lib.eb_sampler_step(pref, B, L, V, eb.EB_BF16, dev_logits.data_ptr(), 0, TEMPERATURE,
+                                 *ptrs, ws.data_ptr(), ws_bytes, sp)
+        if st != 0:
+            raise eb.EbError(st, lib.eb_last_error().decode())
+        for k in out_keys:
+            hout[k].copy_(dstate[k], non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(n):
+        one(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    elapsed = start.elapsed_time(end) / 1e3
+    value, _ = aggregate(n, elapsed, world, dist, local)
+    return {"value": value, "unit": "steps/s", "steps": n, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def cpu_baseline():
+    """The oracle, as it stands, on one full step of the workload (seed 0: 256 rows x
+    262144 bf16, 128 masked) with all its OpenMP threads on the host cores."""
+    import eb_synth
+    import oracle
+    cfg = eb_synth.cfg1(0)
+    x = cfg.logits(0)
+    mask = eb_synth.cfg1_mask(0)
+    st = oracle.State.fresh(B, L, mask)
+    t0 = time.perf_counter()
+    oracle.step(x, st, 0, oracle.Params(seed=0), temperature=float(np.float32(TEMPERATURE)))
+    dt = time.perf_counter() - t0
+    return {"value": 1.0 / dt, "unit": "steps/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "one full step of seed 0 (256 rows x 262144 bf16, 128 masked), all rows "
+                      f"and the selection; {dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world, local):
+    """The oracle as the reference arm: every step is a bounded sample of the workload
+    (R rows of n logits from seed 0, half of them masked), timed on the host cores and
+    scaled to full steps by the element count."""
+    if rank != 0:
+        return
+    import eb_synth
+    import oracle
+    K, W = args.steps, args.warmup
+    R = 16
+    cfg = eb_synth.cfg1(0)
+    masks = eb_synth.cfg1_mask(0)[0]
+    rows = np.concatenate([np.nonzero(masks)[0][:R // 2], np.nonzero(masks == 0)[0][:R // 2]])
+    full = cfg.rows(0, rows, 0)                     # [R, V]
+    params = oracle.Params(seed=0)
+    T = float(np.float32(TEMPERATURE))
+    sub_mask = masks[rows][None, :]
+
+    def run(n):
+        x = np.ascontiguousarray(full[None, :, :n])
+        st = oracle.State.fresh(1, R, sub_mask)
+        t0 = time.perf_counter()
+        oracle.step(x, st, 0, params, temperature=T)
+        return time.perf_counter() - t0
+
+    # size the sample so that K + W steps take about two minutes at most
+    t_full = run(V)
+    budget = 120.0
+    n = V
+    if t_full * (K + W) > budget:
+        n = max(1024, int(V * budget / (t_full * (K + W))) // 8 * 8)
+    for _ in range(W):
+        run(n)
+    times = [run(n) for _ in range(K)]
+    elapsed = sum(times)
+    elems_per_step = R * n
+    value = K * elems_per_step / (B * L * V) / elapsed
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": 1e3 / value,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded Philox / Box-Muller logits, eb_synth)",
+        "config": {"workload": WORKLOAD, "B": B, "L": L, "V": V, "logits_dtype": "bf16",
+                   "masked": 128, "temperature": TEMPERATURE,
+                   "l2": "host cores, not applicable", "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: oracle on {R} rows ({R // 2} masked) x {n} logits "
+                                   f"of seed 0, scaled by {B * L * V}/{elems_per_step} elements"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -81,15 +81,22 @@ def uniform(w) -> np.ndarray:
     return ((w >> np.uint32(9)).astype(_F) + _F(0.5)) * _F(2.0 ** -23)
 
 
-# binary32 constants of the ln / sin / cos series (values of the series coefficients,
-# rounded to binary32)
-_SQRT2 = _F(1.41421356237)
-_C3, _C5, _C7, _C9 = _F(1 / 3), _F(1 / 5), _F(1 / 7), _F(1 / 9)
-_LN2_HI = _F(0.693145751953125)               # 0x3F317200: 16 significant bits
-_LN2_LO = _F(0.6931471805599453 - 0.693145751953125)
-_PI4 = _F(np.pi / 4)
-_S3, _S5, _S7, _S9 = _F(-1 / 6), _F(1 / 120), _F(-1 / 5040), _F(1 / 362880)
-_K2, _K4, _K6, _K8, _K10 = _F(-1 / 2), _F(1 / 24), _F(-1 / 720), _F(1 / 40320), _F(-1 / 3628800)
+# binary32 constants of the ln / sin / cos series, given by bit pattern (they are the
+# series coefficients 1/3, 1/5, ..., -1/6, 1/120, ... and sqrt(2), ln 2, pi/4 rounded to
+# binary32; ln 2 is split Cody-Waite style into a 16-bit head and a tail)
+def _f32bits(b: int) -> np.float32:
+    return np.array([b], np.uint32).view(_F)[0]
+
+
+_SQRT2 = _f32bits(0x3FB504F3)
+_C3, _C5, _C7, _C9 = (_f32bits(0x3EAAAAAB), _f32bits(0x3E4CCCCD), _f32bits(0x3E124925),
+                      _f32bits(0x3DE38E39))
+_LN2_HI, _LN2_LO = _f32bits(0x3F317200), _f32bits(0x35BFBE8E)
+_PI4 = _f32bits(0x3F490FDB)
+_S3, _S5, _S7, _S9 = (_f32bits(0xBE2AAAAB), _f32bits(0x3C088889), _f32bits(0xB9500D01),
+                      _f32bits(0x3638EF1D))
+_K2, _K4, _K6, _K8, _K10 = (_f32bits(0xBF000000), _f32bits(0x3D2AAAAB), _f32bits(0xBAB60B61),
+                            _f32bits(0x37D00D01), _f32bits(0xB493F27E))
 
 
 def _ln(x: np.ndarray) -> np.ndarray:

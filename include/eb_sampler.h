@@ -1,0 +1,171 @@
+/*
+ * eb_sampler.h -- C ABI of the B300 (sm_103a) Entropy-Bounded (EB) denoising sampler of
+ * DiffusionGemma's block-autoregressive text diffusion.
+ *
+ * What one sampler step computes (DiffusionGemma model card, "Best practices" section 1,
+ * "Diffusion sampling settings"; the Korean model card's "Recommendations" section 1 and
+ * the aitrends.kr summary's "Good to know" list say the same):
+ *   1. logit shaping: z = x / T with T linear from t_start = 0.8 (step 0) to t_end = 0.4
+ *      (step max_steps - 1), max_steps = 48;
+ *   2. per canvas position: the full-vocabulary softmax entropy H of z (nats), the
+ *      argmax A of the raw logits (first index on ties) and, for still-masked positions,
+ *      a Gumbel-max sample Y = argmax_v z_v - ln(-ln u_v) with u_v from Philox4x32-10;
+ *   3. adaptive stop (steps >= 1): the mean of H over all L positions is below
+ *      stop_entropy = 0.005 AND A equals the previous step's argmax at every position;
+ *      then every still-masked position takes A and the canvas is done;
+ *   4. otherwise entropy-bounded selection: masked positions sorted by (H, position)
+ *      ascending; sorted index i is accepted iff the sum of the entropies before it is
+ *      <= entropy_bound = 0.1 (index 0 always); accepted positions commit Y, the rest
+ *      stay masked ("fully re-noised");
+ *   5. a canvas whose mask empties is complete; at the last step the positions still
+ *      masked take A (step cap).
+ * The pages give no selection formula; the rule of item 4 is the one this library
+ * implements (the longest sorted prefix whose sum minus its maximum stays within the
+ * bound).
+ *
+ * Conventions shared by every entry point:
+ *   - every d_* pointer is DEVICE memory owned by the caller; the library allocates
+ *     nothing and never synchronises the stream inside eb_sampler_step;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream); all
+ *     work is enqueued asynchronously on it;
+ *   - argument errors return before any launch and leave every buffer untouched;
+ *     eb_last_error() then holds a one-line description (thread-local);
+ *   - device-detected problems never trap: a canvas whose logits hold NaN or +Inf gets
+ *     EB_STATUS_NONFINITE or-ed into its status word and is halted;
+ *   - layouts are row-major: logits [B, L, V] with V contiguous; per-position arrays
+ *     [B, L]; per-canvas arrays [B];
+ *   - tokens use -1 for MASK.
+ */
+#ifndef EB_SAMPLER_H
+#define EB_SAMPLER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EB_OK = 0,
+    EB_ERR_INVALID = 1,      /* bad argument; nothing launched */
+    EB_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed */
+    EB_ERR_UNSUPPORTED = 3,  /* valid but unsupported shape / device */
+    EB_ERR_WORKSPACE = 4,    /* workspace missing or smaller than eb_workspace_bytes() */
+    EB_ERR_CALLBACK = 5      /* the logits callback of eb_sample_canvas returned non-zero */
+} eb_status;
+
+typedef enum { EB_F32 = 0, EB_BF16 = 1 } eb_dtype;
+
+/* Canvas status word d_status[b]: the low byte is the stop reason. */
+#define EB_RUNNING 0
+#define EB_STOP_ADAPTIVE 1       /* mean entropy < stop_entropy and argmax stable */
+#define EB_STOP_COMPLETE 2       /* every position committed by selection */
+#define EB_STOP_CAP 3            /* the last step (max_steps - 1) was reached */
+#define EB_STATUS_NONFINITE 0x100 /* or-ed in: NaN / +Inf logits seen; canvas halted */
+
+typedef struct {
+    int32_t max_steps;     /* 48 */
+    float t_start;         /* 0.8: temperature at step 0 */
+    float t_end;           /* 0.4: temperature at step max_steps - 1 */
+    float entropy_bound;   /* 0.1 */
+    float stop_entropy;    /* 0.005 (strict <) */
+    uint32_t flags;        /* reserved, must be 0 */
+    uint64_t seed;         /* Philox key (low, high 32 bits) of the Gumbel noise */
+} eb_params;
+
+/* Fills *p with the model card's recommended settings (48, 0.8, 0.4, 0.1, 0.005) and
+ * seed 0.  Returns EB_ERR_INVALID on NULL. */
+eb_status eb_default_params(eb_params *p);
+
+/* Temperature of `step` on the linear schedule: t_start + (t_end - t_start) * step /
+ * (max_steps - 1), t_start when max_steps == 1.  Evaluated in binary32. */
+float eb_temperature(const eb_params *p, int step);
+
+/* Bytes of device workspace eb_sampler_step / eb_sample_canvas need for B canvases of L
+ * positions (V and dtype do not change it today but are part of the contract).  The
+ * workspace must be 256-byte aligned; its contents need no initialisation. */
+size_t eb_workspace_bytes(int B, int L, int V, eb_dtype dtype);
+
+/*
+ * One EB sampler step over B canvases (items 1-5 above).
+ *
+ *   params         sampler settings (host pointer, read during the call only)
+ *   B, L, V        canvases, positions per canvas (1..1024), vocabulary (1..2^31-1)
+ *   dtype          element type of d_logits (EB_F32 or EB_BF16)
+ *   d_logits       [B, L, V] logits of this step (read only)
+ *   step           denoising step index s (0-based, < params->max_steps); keys the
+ *                  Gumbel noise and the stop / cap rules
+ *   temperature    > 0: use this T; <= 0: use eb_temperature(params, step)
+ *   d_mask         [B, L] u8 in/out, 1 = masked
+ *   d_tokens       [B, L] i32 in/out, committed token or -1
+ *   d_prev_argmax  [B, L] i32 in/out, argmax of the previous step (-1 before step 0)
+ *   d_status       [B] i32 in/out; canvases whose status is not EB_RUNNING are skipped
+ *   d_steps_taken  [B] i32 out (written when a canvas stops: step + 1); may be NULL
+ *   d_entropy      [B, L] f32 out: H in nats (running canvases only)
+ *   d_argmax       [B, L] i32 out: A
+ *   d_sampled      [B, L] i32 out: Y for masked positions, -1 otherwise
+ *   d_selected     [B, L] u8 out: 1 where a token was committed at this step
+ *   d_committed    [B] i32 out: positions committed at this step; may be NULL
+ *   d_mean_entropy [B] f32 out: mean H of the canvas; may be NULL
+ *   d_workspace    eb_workspace_bytes(B, L, V, dtype) bytes, 256-byte aligned
+ *   stream         cudaStream_t
+ * B == 0 is a no-op.  Returns EB_OK once the work is enqueued.
+ */
+eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                          const void *d_logits, int step, float temperature,
+                          uint8_t *d_mask, int32_t *d_tokens, int32_t *d_prev_argmax,
+                          int32_t *d_status, int32_t *d_steps_taken,
+                          float *d_entropy, int32_t *d_argmax, int32_t *d_sampled,
+                          uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
+                          void *d_workspace, size_t workspace_bytes, void *stream);
+
+/* Logits provider of the denoising loop: enqueue, on `stream`, the logits of `step`
+ * into d_logits [B, L, V] (the denoiser).  It may read d_tokens / d_status (device) to
+ * condition on the canvas and to skip halted canvases.  Returns 0 on success. */
+typedef int (*eb_logits_fn)(void *user, int step, const int32_t *d_tokens,
+                            const int32_t *d_status, void *d_logits, void *stream);
+
+/*
+ * The denoising loop over B independent canvases: for s = start_step .. max_steps-1,
+ * logits_fn(s) then eb_sampler_step(s) with the schedule temperature.  Each canvas
+ * stops on its own (its later steps cost no sampler work); the loop ends early when
+ * every canvas has stopped, checked on the host every `poll_every` steps (0 = never:
+ * run to max_steps; a check copies the B status words back and waits for the stream).  Resuming at
+ * start_step with the state of an earlier call reproduces an uninterrupted run.
+ *
+ *   d_logits            [B, L, V] buffer the callback fills each step
+ *   d_mask .. d_steps_taken   canvas state as in eb_sampler_step (in/out)
+ *   d_committed_per_step [B, max_steps] i32 out or NULL: positions committed at step s
+ *   d_mean_entropy_per_step [B, max_steps] f32 out or NULL: mean H at step s
+ *   d_entropy, d_argmax, d_sampled, d_selected: as in eb_sampler_step, holding the last
+ *                        step's values
+ *   steps_run            host out (may be NULL): sampler steps enqueued
+ * Returns EB_ERR_CALLBACK (after enqueuing nothing further) if logits_fn fails.
+ */
+eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                           eb_logits_fn logits_fn, void *user, void *d_logits, int start_step,
+                           uint8_t *d_mask, int32_t *d_tokens, int32_t *d_prev_argmax,
+                           int32_t *d_status, int32_t *d_steps_taken,
+                           int32_t *d_committed_per_step, float *d_mean_entropy_per_step,
+                           float *d_entropy, int32_t *d_argmax, int32_t *d_sampled,
+                           uint8_t *d_selected, void *d_workspace, size_t workspace_bytes,
+                           int poll_every, int *steps_run, void *stream);
+
+/* Instrumentation: CUDA events (cudaEvent_t as void*) to record on the stream right
+ * before and right after the row-statistics kernel of the NEXT eb_sampler_step /
+ * eb_sample_canvas step enqueued by the calling thread (one-shot; NULL, NULL clears).
+ * Lets a caller time the bandwidth-bound kernel alone with CUDA events. */
+eb_status eb_set_profile_events(void *k1_begin, void *k1_end);
+
+/* Short English name of a status code (static storage). */
+const char *eb_status_string(eb_status s);
+
+/* Description of the last error returned on the calling thread ("" if none). */
+const char *eb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EB_SAMPLER_H */

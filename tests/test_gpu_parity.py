@@ -1,0 +1,360 @@
+"""GPU-vs-oracle parity of the EB sampler step and loop, through the C ABI.
+
+Every input is seeded and synthetic (eb_synth).  The oracle always receives the numpy
+generator's values; the GPU receives the CUDA generator's values, which
+``test_generator_bit_exact`` shows to be the same bits (or an H2D copy of the numpy ones).
+"""
+import numpy as np
+import pytest
+import torch
+
+import canvas_sampler_step_b300 as eb
+import eb_synth
+import eb_synth.device as synth_dev
+import oracle
+from parity import (Report, compare_step, device_logits, host_state, params_pair,
+                    to_device_logits, H_TOL)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    eb.build()
+    synth_dev.build()
+    eb.lib()
+    synth_dev.lib()
+
+
+def _dtype(cfg):
+    return eb.EB_BF16 if cfg.dtype == "bf16" else eb.EB_F32
+
+
+# ------------------------------------------------------------------ generator
+
+@pytest.mark.parametrize("cfg,rows", [
+    (eb_synth.cfg0(0, L=16, V=4096), None),
+    (eb_synth.cfg1(3, L=8, V=262144), None),
+    (eb_synth.Peaked(2, 5, 1001, "f32", 3.0, 1.0, 2.0, (0.3, 0.7), (11, 12)), None),
+    (eb_synth.Peaked(2, 5, 1001, "bf16", 3.0, 1.0, 2.0, (0.3, 0.7), (11, 12)), None),
+    (eb_synth.cfg3(B=8, L=256, V=262144), [0, 77, 255]),
+])
+def test_generator_bit_exact(cfg, rows):
+    for s in (0, 7):
+        dev = device_logits(cfg, s).cpu().numpy()
+        for b in range(cfg.B):
+            p = np.arange(cfg.L) if rows is None else np.array(rows)
+            host = cfg.rows(b, p, s)
+            got = dev[b, p].view(np.uint16) if cfg.dtype == "bf16" else dev[b, p]
+            assert np.array_equal(got.view(np.uint32 if cfg.dtype == "f32" else np.uint16),
+                                  host.view(np.uint32 if cfg.dtype == "f32" else np.uint16)), (b, s)
+
+
+def test_generator_skips_stopped_canvases():
+    cfg = eb_synth.cfg3(B=4, L=4, V=64)
+    out = torch.full((4, 4, 64), 7, dtype=torch.int16, device="cuda")
+    status = torch.tensor([0, 1, 0, 2], dtype=torch.int32, device="cuda")
+    synth_dev.logits(synth_dev.Recipe.of(cfg), 3, out, status)
+    o = out.cpu().numpy()
+    assert (o[1] == 7).all() and (o[3] == 7).all() and not (o[0] == 7).all()
+
+
+# ------------------------------------------------------------------ one step
+
+def _run_step(cfg, step, mask=None, seed=5, temperature=0.0, state=None, **kw):
+    gp, op = params_pair(seed=seed, **kw)
+    x = cfg.logits(step)
+    c = eb.Canvas(cfg.B, cfg.L, cfg.V, _dtype(cfg), mask=mask)
+    ost = oracle.State.fresh(cfg.B, cfg.L, mask)
+    if state is not None:
+        state(c, ost)
+    running = ost.status == oracle.RUNNING
+    c.step(gp, to_device_logits(x), step, temperature)
+    res = oracle.step(x, ost, step, op, temperature=float(np.float32(temperature)))
+    return host_state(c), res, ost, running
+
+
+CASES = [
+    # (recipe, step, mask density)  -- vector paths, several tiles per row, ragged tails
+    (eb_synth.cfg0(0, L=256, V=4096), 0, 1.0),
+    (eb_synth.cfg0(0, L=256, V=4096), 9, 0.7),
+    (eb_synth.Peaked(3, 64, 20000, "bf16", 2.5, 0.0, 12.0, (0.0, 0.0, 0.0), (1, 2, 3)), 0, 0.5),
+    (eb_synth.Peaked(2, 100, 2048, "bf16", 3.0, 4.0, 2.0, (0.3, 0.3), (4, 5)), 20, 0.8),
+    # scalar paths: V not a multiple of the 16-byte vector
+    (eb_synth.Peaked(2, 16, 4099, "f32", 3.0, 2.0, 0.0, (0.3, 0.3), (6, 7)), 3, 1.0),
+    (eb_synth.Peaked(1, 40, 12347, "bf16", 2.5, 0.0, 12.0, (0.0,), (8,)), 0, 0.5),
+    # tiny rows and a non-power-of-two canvas
+    (eb_synth.Peaked(1, 1000, 8, "f32", 1.0, 3.0, 0.0, (0.0,), (9,)), 2, 0.9),
+    (eb_synth.Peaked(4, 1, 1, "f32", 1.0, 0.0, 0.0, (0.0,) * 4, (1, 2, 3, 4)), 0, 1.0),
+]
+
+
+@pytest.mark.parametrize("cfg,step,density", CASES)
+def test_step_parity(cfg, step, density):
+    rng = np.random.default_rng(step + cfg.V)
+    mask = (rng.random((cfg.B, cfg.L)) < density).astype(np.uint8)
+    mask[:, 0] = 1
+    g, res, ost, running = _run_step(cfg, step, mask=mask)
+    rep = Report()
+    compare_step(g, res, ost, running, rep, ctx=f"V={cfg.V}")
+    assert rep.canvas_ties <= max(1, cfg.B // 4)
+
+
+def test_step_parity_low_entropy_many_accepted():
+    # peaks so high that most entropies are ~0: selection accepts long prefixes
+    cfg = eb_synth.Peaked(2, 256, 4096, "f32", 1.0, 30.0, 10.0, (0.0, 0.0), (3, 4))
+    g, res, ost, running = _run_step(cfg, 4)
+    rep = Report()
+    compare_step(g, res, ost, running, rep)
+    assert res.committed.min() > 1
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_step_parity_single_step_workload_full_size(seed):
+    """B=1, L=256, V=262144 bf16, 128 of 256 masked, T=0.8 (the benchmarked step)."""
+    cfg = eb_synth.cfg1(seed)
+    mask = eb_synth.cfg1_mask(seed)
+    x = cfg.logits(0)
+    dev = device_logits(cfg, 0)
+    assert torch.equal(dev.cpu(), torch.from_numpy(x.view(np.int16)))
+    gp, op = params_pair(seed=seed)
+    c = eb.Canvas(1, 256, 262144, eb.EB_BF16, mask=mask)
+    ost = oracle.State.fresh(1, 256, mask)
+    c.step(gp, dev, 0, 0.8)
+    res = oracle.step(x, ost, 0, op, temperature=float(np.float32(0.8)))
+    rep = Report()
+    compare_step(host_state(c), res, ost, np.array([True]), rep, ctx=f"seed {seed}")
+    assert rep.max_h_err < H_TOL
+
+
+# ------------------------------------------------------------------ the loop
+
+def _lockstep(cfg, params_kw=None, mask=None, sampled_rows=None, max_compare_steps=None):
+    """Run eb_sampler_step step by step next to the oracle; return (reports, gpu history)."""
+    gp, op = params_pair(seed=cfg.seeds[0], **(params_kw or {}))
+    c = eb.Canvas(cfg.B, cfg.L, cfg.V, _dtype(cfg), mask=mask, max_steps=gp.max_steps)
+    ost = oracle.State.fresh(cfg.B, cfg.L, mask)
+    rep = Report()
+    hist = []
+    for s in range(gp.max_steps):
+        st_before = c.status.cpu().numpy()
+        if not (st_before == eb.EB_RUNNING).any():
+            break
+        dev = device_logits(cfg, s, c.status)
+        c.step(gp, dev, s, 0.0)
+        g = host_state(c)
+        hist.append(g)
+        if max_compare_steps is not None and s >= max_compare_steps:
+            continue
+        running = ost.status == oracle.RUNNING
+        if not np.array_equal(running, st_before == eb.EB_RUNNING):
+            break      # trajectories parted after a counted tie
+        x = cfg.logits(s)
+        res = oracle.step(x, ost, s, op)
+        tied = compare_step(g, res, ost, running, rep, ctx=f"step {s}")
+        if tied:
+            break
+    return rep, hist, c
+
+
+def test_loop_parity_pr1_workload():
+    """B=1, L=256, V=4096 fp32, up to 48 steps, seed 0: lockstep with the oracle."""
+    cfg = eb_synth.cfg0(0)
+    rep, hist, c = _lockstep(cfg)
+    assert rep.canvases >= 10
+    # the whole loop through eb_sample_canvas reproduces the stepwise run bit for bit
+    gp, _ = params_pair(seed=0)
+    c2 = eb.Canvas(1, 256, 4096, eb.EB_F32, max_steps=48)
+    buf = torch.empty((1, 256, 4096), dtype=torch.float32, device="cuda")
+    recipe = synth_dev.Recipe.of(cfg)
+    import ctypes
+    ran = c2.run(gp, synth_dev.callback_address(), ctypes.addressof(recipe), buf)
+    g2 = host_state(c2)
+    last = hist[-1]
+    for k in ("tokens", "mask", "status", "steps_taken", "prev_argmax"):
+        assert np.array_equal(g2[k], last[k]), k
+    assert ran == 48 or g2["status"][0] != eb.EB_RUNNING
+    assert g2["mask"].sum() == 0 and (g2["tokens"] >= 0).all()
+
+
+def test_loop_parity_mixed_batch_small():
+    """B=8 canvases with per-canvas growth rates (easy / hard), V=2048 bf16."""
+    cfg = eb_synth.Peaked(8, 64, 2048, "bf16", 3.0, 0.0, 4.0, eb_synth.cfg3().growth,
+                          tuple(range(8)))
+    rep, hist, c = _lockstep(cfg)
+    st = hist[-1]["status"]
+    assert (st != eb.EB_RUNNING).all()
+    assert rep.canvases > 50
+
+
+def _check_selection_properties(g, mask_before, bound=np.float32(0.1)):
+    """Selection validity from the GPU's own entropies: the committed masked positions
+    are the k lowest (H, p) and k follows the prefix rule (up to the tie window)."""
+    B, L = g["entropy"].shape
+    for b in range(B):
+        m = mask_before[b].astype(bool)
+        if not m.any() or g["status"][b] in (eb.EB_STOP_ADAPTIVE, eb.EB_STOP_CAP):
+            continue
+        idx = np.nonzero(m)[0]
+        order = idx[np.lexsort((idx, g["entropy"][b][idx]))]
+        Hs = g["entropy"][b][order].astype(np.float64)
+        before = np.concatenate([[0.0], np.cumsum(Hs)[:-1]])
+        k = int(np.sum((np.arange(len(order)) == 0) | (before <= float(bound))))
+        sel = np.nonzero(g["selected"][b])[0]
+        if np.min(np.abs(before[1:] - float(bound)), initial=1.0) < 1e-5:
+            continue
+        assert sorted(sel.tolist()) == sorted(order[:k].tolist())
+
+
+def test_loop_full_size_batch_of_eight():
+    """B=8, L=256, V=262144 bf16, rates (0.1, 0.2, 0.4, 0.8), up to 48 steps: sampled rows
+    vs the oracle at every step, selection properties from the GPU's own entropies, and
+    eb_sample_canvas equal to the stepwise run."""
+    cfg = eb_synth.cfg3()
+    gp, op = params_pair(seed=0)
+    c = eb.Canvas(8, 256, 262144, eb.EB_BF16, max_steps=48)
+    rng = np.random.default_rng(0)
+    checked = 0
+    hist = []
+    for s in range(48):
+        st_before = c.status.cpu().numpy()
+        if not (st_before == 0).any():
+            break
+        mask_before = c.mask.cpu().numpy()
+        dev = device_logits(cfg, s, c.status)
+        c.step(gp, dev, s, 0.0)
+        g = host_state(c)
+        hist.append(g)
+        _check_selection_properties(g, mask_before)
+        if s % 6 == 0:
+            T = oracle.temperature(s, 48, op.t_start, op.t_end)
+            for b in np.nonzero(st_before == 0)[0][:3]:
+                for p in rng.choice(256, 2, replace=False):
+                    x = cfg.rows(int(b), np.array([p]), s)[0]
+                    H, A, Y, gap = oracle.row(x, T, bool(mask_before[b, p]), 0, int(b), int(p), s)
+                    assert abs(g["entropy"][b, p] - H) <= H_TOL
+                    assert g["argmax"][b, p] == A
+                    if mask_before[b, p] and gap >= 1e-6:
+                        assert g["sampled"][b, p] == Y
+                    checked += 1
+    assert checked >= 20
+    final = hist[-1]
+    assert (final["status"] != 0).all() and final["mask"].sum() == 0
+    # the same loop in one call
+    c2 = eb.Canvas(8, 256, 262144, eb.EB_BF16, max_steps=48)
+    buf = torch.empty((8, 256, 262144), dtype=torch.int16, device="cuda")
+    recipe = synth_dev.Recipe.of(cfg)
+    import ctypes
+    c2.run(gp, synth_dev.callback_address(), ctypes.addressof(recipe), buf, poll_every=4)
+    g2 = host_state(c2)
+    for k in ("tokens", "status", "steps_taken"):
+        assert np.array_equal(g2[k], final[k]), k
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_empty_batch_is_noop():
+    gp, _ = params_pair()
+    eb.eb_sampler_step(gp, 0, 256, 4096, eb.EB_F32, None, 0, 0.0, None, None, None, None, None,
+                       None, None, None, None, None, None, None, 0)
+
+
+def test_all_unmasked_canvas_completes_without_commit():
+    cfg = eb_synth.cfg0(0, L=32, V=512)
+    g, res, ost, running = _run_step(cfg, 0, mask=np.zeros((1, 32), np.uint8))
+    assert g["status"][0] == eb.EB_STOP_COMPLETE and g["committed"][0] == 0
+    assert (g["sampled"] == -1).all()
+    rep = Report()
+    compare_step(g, res, ost, running, rep)
+
+
+def test_stopped_canvases_untouched():
+    cfg = eb_synth.Peaked(3, 16, 256, "f32", 2.0, 1.0, 0.0, (0.0,) * 3, (1, 1, 1))
+
+    def prep(c, ost):
+        c.status[1] = eb.EB_STOP_CAP
+        ost.status[1] = oracle.CAP
+    g, res, ost, running = _run_step(cfg, 1, state=prep)
+    assert g["status"][1] == eb.EB_STOP_CAP and (g["mask"][1] == 1).all()
+    rep = Report()
+    compare_step(g, res, ost, running, rep)
+
+
+def test_nonfinite_logits_set_status_bit():
+    for bad in (np.nan, np.inf):
+        x = np.zeros((2, 8, 64), np.float32)
+        x[1, 3, 5] = bad
+        c = eb.Canvas(2, 8, 64, eb.EB_F32)
+        gp, _ = params_pair()
+        c.step(gp, to_device_logits(x), 0, 0.0)
+        g = host_state(c)
+        assert g["status"][1] & eb.EB_STATUS_NONFINITE
+        assert g["status"][0] == eb.EB_RUNNING
+
+
+def test_minus_inf_logits_k_point_entropy():
+    # k equal top logits and the rest -inf: H = ln k, sample among the k, argmax = first
+    x = np.full((1, 4, 4096), -np.inf, np.float32)
+    tops = {0: [5], 1: [7, 900], 2: [1, 2, 3], 3: list(range(100, 4096, 64))}
+    for p, t in tops.items():
+        x[0, p, t] = 1.5
+    c = eb.Canvas(1, 4, 4096, eb.EB_F32)
+    gp, _ = params_pair(entropy_bound=-1.0)
+    c.step(gp, to_device_logits(x), 0, 0.0)
+    g = host_state(c)
+    for p, t in tops.items():
+        assert abs(g["entropy"][0, p] - np.log(len(t))) < H_TOL
+        assert g["argmax"][0, p] == t[0]
+        assert g["sampled"][0, p] in t
+
+
+def test_deterministic_repeat():
+    cfg = eb_synth.Peaked(2, 64, 50000, "bf16", 2.5, 0.0, 12.0, (0.0, 0.0), (1, 2))
+    x = to_device_logits(cfg.logits(0))
+    outs = []
+    for _ in range(2):
+        c = eb.Canvas(2, 64, 50000, eb.EB_BF16)
+        gp, _ = params_pair(seed=3)
+        c.step(gp, x, 0, 0.8)
+        outs.append(host_state(c))
+    for k in outs[0]:
+        assert np.array_equal(outs[0][k], outs[1][k], equal_nan=True), k
+
+
+def test_callback_failure_aborts_loop():
+    c = eb.Canvas(1, 8, 64, eb.EB_F32)
+    buf = torch.zeros((1, 8, 64), dtype=torch.float32, device="cuda")
+    calls = []
+
+    @eb.LOGITS_FN
+    def fn(user, step, tokens, status, logits, stream):
+        calls.append(step)
+        return 0 if step < 2 else 1
+
+    gp, _ = params_pair()
+    with pytest.raises(eb.EbError) as ei:
+        c.run(gp, fn, None, buf)
+    assert ei.value.status == eb.EB_ERR_CALLBACK
+    assert calls == [0, 1, 2]
+
+
+def test_resume_reproduces_uninterrupted_run():
+    cfg = eb_synth.cfg0(1, L=64, V=1024)
+    recipe = synth_dev.Recipe.of(cfg)
+    import ctypes
+    gp, _ = params_pair(seed=1, max_steps=12)
+    buf = torch.empty((1, 64, 1024), dtype=torch.float32, device="cuda")
+    full = eb.Canvas(1, 64, 1024, eb.EB_F32, max_steps=12)
+    full.run(gp, synth_dev.callback_address(), ctypes.addressof(recipe), buf)
+    part = eb.Canvas(1, 64, 1024, eb.EB_F32, max_steps=12)
+    gp5, _ = params_pair(seed=1, max_steps=12)
+    # first 5 steps via the step API, then resume the loop at step 5
+    for s in range(5):
+        synth_dev.logits(recipe, s, buf, part.status)
+        part.step(gp5, buf, s)
+    part.run(gp, synth_dev.callback_address(), ctypes.addressof(recipe), buf, start_step=5)
+    a, b = host_state(full), host_state(part)
+    for k in ("tokens", "status", "steps_taken", "prev_argmax"):
+        assert np.array_equal(a[k], b[k]), k

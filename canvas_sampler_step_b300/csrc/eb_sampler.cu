@@ -1,28 +1,6 @@
-// eb_sampler.cu -- B300 (sm_103a) kernels and C ABI of the Entropy-Bounded (EB) denoising
-// sampler step of DiffusionGemma (model card, "Best practices" section 1, "Diffusion
-// sampling settings": 48 steps, temperature 0.8 -> 0.4 for logit shaping, lowest-entropy
-// selection under the entropy bound 0.1, full re-noising of the unselected tokens,
-// adaptive stop at mean entropy < 0.005 with an argmax stable over two steps).
-//
-// Two kernels per step:
-//   k1_rowstats  streams the [B, L, V] logits once.  The flattened (row, 16-byte vector)
-//                index space is cut into G equal contiguous ranges, one per CTA (G = SMs x
-//                resident CTAs), so every CTA moves the same number of bytes.  Each thread
-//                keeps an online state per row segment: the running raw max xm and its first
-//                index, S = sum 2^t and T2 = sum t 2^t with t = (x - xm) log2(e) / T, and for
-//                masked rows the best Gumbel score.  A CTA writes one partial state per row
-//                segment it touched to slot (row + cta) of the workspace.
-//   k2_select    one CTA per canvas: merges the partials of its rows in a fixed order
-//                (deterministic), forms H = ln2 (log2 S - T2 / S), runs the stop test, the
-//                entropy-bounded selection (bitonic sort of (H, position) keys, prefix sums
-//                in binary64), commits / re-masks and finalises complete / capped canvases.
-//
-// Gumbel-max without a log per entry: with E_v = -ln u_v the sample is the v maximising
-// z_v - ln E_v.  Since E_v >= delta_v = 1 - u_v (exact from the Philox word), an entry can
-// only beat the current best score `best` if delta_v < 2^t_v * 2^(xm log2e / T - best
-// log2e).  That test costs one multiply and compare per entry; only entries that pass it
-// (a handful per warp and row) evaluate the exact score with log1pf / logf.  The best score
-// is shared across the warp whenever it improves, which keeps the pass rate low.
+// eb_sampler.cu -- kernels and C ABI of the B300 (sm_103a) Entropy-Bounded (EB) denoising
+// sampler step of DiffusionGemma.  The algorithm and the kernel structure are described at
+// the top of eb_kernels.cuh.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -33,205 +11,17 @@
 #include <cstring>
 #include <string>
 
+#include "eb_kernels.cuh"
 #include "eb_sampler.h"
 
 namespace ebk {
-
-constexpr int kK1Threads = 256;
-constexpr int kK1Unroll = 4;
-constexpr int kK2Threads = 256;
-constexpr int kMaxL = 1024;
-constexpr int kMaxGrid = 8192;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kEmptyMax = -1.0e30f;     // running max of a slice that saw no element
-constexpr float kMinT = -16384.0f;        // log2-domain clamp: 2^t is exactly 0 below it
-constexpr float kCandSlack = 1.0f + 1.0f / 256.0f;
-constexpr float kOneMinusHalfUlp = 0.99999994039535522f;  // 1 - 2^-24
-constexpr uint32_t kStreamGumbel = 1u;
-
-// Philox4x32-10 round keys (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85), r = 0..9; computed
-// on the host and passed as a kernel parameter so that each xor reads the constant bank.
-struct RoundKeys {
-    uint32_t k[20];
-};
-
-// Per-(row, CTA) partial state.  xm: max raw logit of the slice (kEmptyMax if empty);
-// S, T2: sums of 2^t and t 2^t, t = (x - xm) c, c = log2(e) / T; ai: first index of xm;
-// best / bi: best Gumbel score z - ln E and its index (-inf / -1 if none).
-struct __align__(16) Partial {
-    float xm, S, T2;
-    int ai;
-    float best;
-    int bi;
-    int pad0, pad1;
-};
-
-struct RowState {
-    float xm, S, T2;
-    int ai;
-    float best;
-    int bi;
-};
-
-struct K1Args {
-    const void *logits;
-    const uint8_t *mask;
-    const int32_t *status;
-    Partial *partials;
-    long long nvec_row;  // vectors (16 B, or 1 element on the scalar path) per row
-    long long N;         // rows * nvec_row
-    int L;
-    int G;
-    int step;
-    float c;             // log2(e) / T
-    float invT;          // 1 / T
-    RoundKeys keys;
-};
-
-struct K2Args {
-    const Partial *partials;
-    uint8_t *mask;
-    int32_t *tokens;
-    int32_t *prev_argmax;
-    int32_t *status;
-    int32_t *steps_taken;
-    float *entropy;
-    int32_t *argmax;
-    int32_t *sampled;
-    uint8_t *selected;
-    int32_t *committed;        // [B] or null
-    float *mean_entropy;       // [B] or null
-    int32_t *committed_hist;   // [B, max_steps] or null
-    float *mean_hist;          // [B, max_steps] or null
-    long long nvec_row;
-    long long N;
-    int L;
-    int G;
-    int step;
-    int max_steps;
-    float c;
-    float bound;
-    float stop_entropy;
-};
-
-// ------------------------------------------------------------------ device helpers
-
-__device__ __forceinline__ float ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint4 ldg_stream(const uint4 *p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-// Philox4x32-10 (Salmon et al., SC'11): two 32x32->64 products per round, high halves
-// xored with the other counter words and the round key.
-__device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                        const RoundKeys &K)
-{
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
-        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
-        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ K.k[2 * r];
-        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ K.k[2 * r + 1];
-        c1 = (uint32_t)p1;
-        c3 = (uint32_t)p0;
-        c0 = n0;
-        c2 = n2;
-    }
-    return make_uint4(c0, c1, c2, c3);
-}
-
-// delta = 1 - u for the uniform u = (j + 1/2) 2^-23, j = low 23 bits of w; exact.
-__device__ __forceinline__ float gumbel_delta(uint32_t w)
-{
-    return __uint_as_float((w & 0x7FFFFFu) ^ 0x3FFFFFFFu) - kOneMinusHalfUlp;
-}
-
-__device__ __forceinline__ float cand_scale(float xm, float best, float c)
-{
-    return ex2(fmaf(xm, c, -best * kLog2e)) * kCandSlack;
-}
-
-__device__ __forceinline__ bool better(float s, int i, float bs, int bi)
-{
-    return s > bs || (s == bs && (unsigned)i < (unsigned)bi);
-}
-
-// Associative merge of two online states (c = log2(e) / T).
-__device__ __forceinline__ void merge_state(RowState &a, float xm, float S, float T2, int ai,
-                                            float best, int bi, float c)
-{
-    const float m = fmaxf(a.xm, xm);
-    const float da = (a.xm - m) * c;
-    const float db = (xm - m) * c;
-    const float sa = ex2(da), sb = ex2(db);
-    const float T2n = sa * fmaf(da, a.S, a.T2) + sb * fmaf(db, S, T2);
-    const float Sn = a.S * sa + S * sb;
-    int ain;
-    if (a.xm > xm) ain = a.ai;
-    else if (xm > a.xm) ain = ai;
-    else ain = min(a.ai, ai);
-    a.xm = m;
-    a.S = Sn;
-    a.T2 = T2n;
-    a.ai = ain;
-    if (better(best, bi, a.best, a.bi)) {
-        a.best = best;
-        a.bi = bi;
-    }
-}
-
-__device__ __forceinline__ void warp_merge(RowState &st, float c)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float xm = __shfl_xor_sync(0xFFFFFFFFu, st.xm, off);
-        const float S = __shfl_xor_sync(0xFFFFFFFFu, st.S, off);
-        const float T2 = __shfl_xor_sync(0xFFFFFFFFu, st.T2, off);
-        const int ai = __shfl_xor_sync(0xFFFFFFFFu, st.ai, off);
-        const float best = __shfl_xor_sync(0xFFFFFFFFu, st.best, off);
-        const int bi = __shfl_xor_sync(0xFFFFFFFFu, st.bi, off);
-        merge_state(st, xm, S, T2, ai, best, bi, c);
-    }
-}
-
-__device__ __forceinline__ void warp_best(float &best, int &bi)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (better(ob, oi, best, bi)) {
-            best = ob;
-            bi = oi;
-        }
-    }
-}
-
-// ------------------------------------------------------------------ element kinds
 
 enum Kind { kF32Vec = 0, kBF16Vec = 1, kF32Scalar = 2, kBF16Scalar = 3 };
 
 template <int KIND> struct KindTraits;
 template <> struct KindTraits<kF32Vec> {
     static constexpr int VEC = 4;
-    using Raw = uint4;
-    static __device__ __forceinline__ Raw load(const void *row, long long i)
-    {
-        return ldg_stream(reinterpret_cast<const uint4 *>(row) + i);
-    }
-    static __device__ __forceinline__ void unpack(const Raw &r, float (&x)[4])
+    static __device__ __forceinline__ void unpack(const uint4 &r, float (&x)[4])
     {
         x[0] = __uint_as_float(r.x);
         x[1] = __uint_as_float(r.y);
@@ -241,12 +31,7 @@ template <> struct KindTraits<kF32Vec> {
 };
 template <> struct KindTraits<kBF16Vec> {
     static constexpr int VEC = 8;
-    using Raw = uint4;
-    static __device__ __forceinline__ Raw load(const void *row, long long i)
-    {
-        return ldg_stream(reinterpret_cast<const uint4 *>(row) + i);
-    }
-    static __device__ __forceinline__ void unpack(const Raw &r, float (&x)[8])
+    static __device__ __forceinline__ void unpack(const uint4 &r, float (&x)[8])
     {
         x[0] = __uint_as_float(r.x << 16);
         x[1] = __uint_as_float(r.x & 0xFFFF0000u);
@@ -258,386 +43,614 @@ template <> struct KindTraits<kBF16Vec> {
         x[7] = __uint_as_float(r.w & 0xFFFF0000u);
     }
 };
-template <> struct KindTraits<kF32Scalar> {
-    static constexpr int VEC = 1;
-    using Raw = float;
-    static __device__ __forceinline__ Raw load(const void *row, long long i)
-    {
-        return __ldg(reinterpret_cast<const float *>(row) + i);
-    }
-    static __device__ __forceinline__ void unpack(const Raw &r, float (&x)[1]) { x[0] = r; }
-};
-template <> struct KindTraits<kBF16Scalar> {
-    static constexpr int VEC = 1;
-    using Raw = unsigned short;
-    static __device__ __forceinline__ Raw load(const void *row, long long i)
-    {
-        return __ldg(reinterpret_cast<const unsigned short *>(row) + i);
-    }
-    static __device__ __forceinline__ void unpack(const Raw &r, float (&x)[1])
-    {
-        x[0] = __uint_as_float((uint32_t)r << 16);
-    }
-};
 
-template <int KIND> __host__ __device__ constexpr int elem_bytes()
-{
-    return (KIND == kF32Vec || KIND == kF32Scalar) ? 4 : 2;
-}
-
-// Philox words of the VEC entries starting at vector index i (entry v0 = i * VEC).
+// Philox words of the VEC entries of vector jvec (entries jvec*VEC ..).  The word of entry
+// v is word v % 4 of counter (v / 4, p, s, stream << 24 | b).
 template <int VEC>
-__device__ __forceinline__ void gumbel_words(long long i, uint32_t p, uint32_t s, uint32_t sw,
+__device__ __forceinline__ void gumbel_words(long long jvec, uint32_t p, uint32_t s, uint32_t sw,
                                              const RoundKeys &K, uint32_t (&w)[VEC])
 {
     if constexpr (VEC == 8) {
-        const uint4 a = philox((uint32_t)(2 * i), p, s, sw, K);
-        const uint4 b = philox((uint32_t)(2 * i + 1), p, s, sw, K);
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        const uint4 u = philox((uint32_t)(2 * jvec), p, s, sw, K);
+        const uint4 v = philox((uint32_t)(2 * jvec + 1), p, s, sw, K);
+        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+        w[4] = v.x; w[5] = v.y; w[6] = v.z; w[7] = v.w;
     } else if constexpr (VEC == 4) {
-        const uint4 a = philox((uint32_t)i, p, s, sw, K);
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        const uint4 u = philox((uint32_t)jvec, p, s, sw, K);
+        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
     } else {
-        const uint4 a = philox((uint32_t)(i >> 2), p, s, sw, K);
-        const uint32_t q = (uint32_t)(i & 3);
-        w[0] = q == 0 ? a.x : (q == 1 ? a.y : (q == 2 ? a.z : a.w));
+        const uint4 u = philox((uint32_t)(jvec >> 2), p, s, sw, K);
+        const uint32_t q = (uint32_t)(jvec & 3);
+        w[0] = q == 0 ? u.x : (q == 1 ? u.y : (q == 2 ? u.z : u.w));
     }
 }
 
-// One row segment [i0, i1) (vector indices within row r) by the whole CTA.
-template <int KIND, bool MASKED>
-__device__ __forceinline__ void k1_segment_loop(const K1Args &a, const void *rowp, long long i0,
-                                                long long i1, uint32_t p, uint32_t sw,
-                                                RowState &st)
+// One vector of VEC logits (entries jvec*VEC ..).  Every lane of the warp calls this with
+// the same trip count; `valid` masks lanes without a vector.
+template <int VEC, bool MASKED>
+__device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, long long jvec,
+                                            const K1Args &a, uint32_t p, uint32_t sw,
+                                            RowState &st, float &nb, float &K)
 {
-    using T = KindTraits<KIND>;
-    constexpr int VEC = T::VEC;
-    const int tid = threadIdx.x;
-    float nb = -st.xm * a.c;
-    float K = MASKED ? cand_scale(st.xm, st.best, a.c) : 0.0f;
-    for (long long base = i0; base < i1; base += (long long)kK1Threads * kK1Unroll) {
-        typename T::Raw raw[kK1Unroll];
-        bool valid[kK1Unroll];
+    float e[VEC];
+    if (valid) {
+        float vmax;
+        if constexpr (VEC == 8) vmax = max3(max3(x[0], x[1], x[2]), max3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+        else if constexpr (VEC == 4) vmax = max3(x[0], x[1], fmaxf(x[2], x[3]));
+        else vmax = x[0];
+        if (vmax > st.xm) {
+            // new running max: rescale the sums and take its first index as the argmax
+            const float d = (st.xm - vmax) * a.c;
+            const float sc = ex2(d);
+            st.T2 = sc * fmaf(d, st.S, st.T2);
+            st.S *= sc;
+            int j0 = VEC - 1;
 #pragma unroll
-        for (int u = 0; u < kK1Unroll; ++u) {
-            const long long i = base + (long long)u * kK1Threads + tid;
-            valid[u] = i < i1;
-            if (valid[u]) raw[u] = T::load(rowp, i);
+            for (int j = VEC - 1; j >= 0; --j)
+                if (x[j] == vmax) j0 = j;
+            st.ai = (int)(jvec * VEC + j0);
+            st.xm = vmax;
+            nb = -vmax * a.c;
+            if (MASKED) K = cand_scale(st.xm, st.best, a.c);
         }
 #pragma unroll
-        for (int u = 0; u < kK1Unroll; ++u) {
-            const long long i = base + (long long)u * kK1Threads + tid;
-            float x[VEC];
-            float e[VEC];
-            if (valid[u]) {
-                T::unpack(raw[u], x);
-                float vmax = x[0];
+        for (int j = 0; j < VEC; ++j) {
+            const float t = fmaf(x[j], a.c, nb);
+            e[j] = ex2(t);
+            st.S += e[j];
+            st.T2 = fmaf(t, e[j], st.T2);
+        }
+    }
+    if constexpr (MASKED) {
+        uint32_t w[VEC];
+        bool any = false;
+        if (valid) {
+            gumbel_words<VEC>(jvec, p, (uint32_t)a.step, sw, a.keys, w);
 #pragma unroll
-                for (int j = 1; j < VEC; ++j) vmax = fmaxf(vmax, x[j]);
-                if (vmax > st.xm) {
-                    const float d = (st.xm - vmax) * a.c;
-                    const float sc = ex2(d);
-                    st.T2 = sc * fmaf(d, st.S, st.T2);
-                    st.S *= sc;
-                    int j0 = VEC - 1;
-#pragma unroll
-                    for (int j = VEC - 1; j >= 0; --j)
-                        if (x[j] == vmax) j0 = j;
-                    st.ai = (int)(i * VEC + j0);
-                    st.xm = vmax;
-                    nb = -vmax * a.c;
-                    if (MASKED) K = cand_scale(st.xm, st.best, a.c);
-                }
+            for (int j = 0; j < VEC; ++j) any |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
+        }
+        if (__any_sync(0xFFFFFFFFu, any)) {
+            if (any) {
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
-                    const float t = fmaxf(fmaf(x[j], a.c, nb), kMinT);
-                    e[j] = ex2(t);
-                    st.S += e[j];
-                    st.T2 = fmaf(t, e[j], st.T2);
-                }
-            }
-            if constexpr (MASKED) {
-                uint32_t cand = 0;
-                uint32_t w[VEC];
-                if (valid[u]) {
-                    gumbel_words<VEC>(i, p, (uint32_t)a.step, sw, a.keys, w);
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        if (e[j] * K > gumbel_delta(w[j])) cand |= 1u << j;
-                }
-                if (__any_sync(0xFFFFFFFFu, cand != 0)) {
-                    while (cand) {
-                        const int j = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        float xj = x[0];
-                        uint32_t wj = w[0];
-#pragma unroll
-                        for (int q = 1; q < VEC; ++q)
-                            if (q == j) { xj = x[q]; wj = w[q]; }
-                        const float E = -log1pf(-gumbel_delta(wj));
-                        const float score = xj * a.invT - logf(E);
-                        const int idx = (int)(i * VEC + j);
+                    const float f = one_minus_u_plus(w[j]);
+                    if (f < fmaf(e[j], K, kCandAdd)) {
+                        const float delta = f - kOneMinusHalfUlp;          // 1 - u, exact
+                        const float E = -log1pf(-delta);                   // -ln u
+                        const float score = x[j] * a.invT - logf(E);
+                        const int idx = (int)(jvec * VEC + j);
                         if (better(score, idx, st.best, st.bi)) {
                             st.best = score;
                             st.bi = idx;
                         }
                     }
-                    warp_best(st.best, st.bi);
-                    K = cand_scale(st.xm, st.best, a.c);
                 }
             }
+            warp_best(st.best, st.bi);
+            K = cand_scale(st.xm, st.best, a.c);
         }
     }
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(kK1Threads) k1_rowstats(const K1Args a)
+// Builds the weight prefix P[0..rows] (and the per-row mask flags) in shared memory with
+// all threads of the block.  Row weight: 0 for halted canvases, nvec * (masked ? w_m : w_u).
+__device__ void build_prefix(const K1Args &a, uint32_t *P, uint8_t *mflag, uint32_t *scan)
 {
-    using T = KindTraits<KIND>;
-    __shared__ RowState red[kK1Threads / 32];
-    const int cta = blockIdx.x;
-    const long long lo = (long long)cta * a.N / a.G;
-    const long long hi = (long long)(cta + 1) * a.N / a.G;
-    const size_t row_bytes = (size_t)a.nvec_row * T::VEC * elem_bytes<KIND>();
-    long long seg = lo;
-    while (seg < hi) {
-        const long long r = seg / a.nvec_row;
-        const long long rend = min(hi, (r + 1) * a.nvec_row);
-        const long long i0 = seg - r * a.nvec_row;
-        const long long i1 = rend - r * a.nvec_row;
-        seg = rend;
-        const int b = (int)(r / a.L);
-        const uint32_t p = (uint32_t)(r - (long long)b * a.L);
-        if (a.status[b] != EB_RUNNING) continue;   // CTA-uniform
-        const bool masked = a.mask[r] != 0;
-        const void *rowp = static_cast<const char *>(a.logits) + (size_t)r * row_bytes;
-        const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
-        RowState st{kEmptyMax, 0.0f, 0.0f, 0, -INFINITY, -1};
-        if (masked) k1_segment_loop<KIND, true>(a, rowp, i0, i1, p, sw, st);
-        else k1_segment_loop<KIND, false>(a, rowp, i0, i1, p, sw, st);
-        warp_merge(st, a.c);
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (lane == 0) red[warp] = st;
-        __syncthreads();
-        if (warp == 0) {
-            RowState s2 = lane < kK1Threads / 32 ? red[lane]
-                                                 : RowState{kEmptyMax, 0.0f, 0.0f, 0x7FFFFFFF,
-                                                            -INFINITY, -1};
-            warp_merge(s2, a.c);
-            if (lane == 0) {
-                Partial out;
-                out.xm = s2.xm;
-                out.S = s2.S;
-                out.T2 = s2.T2;
-                out.ai = s2.ai;
-                out.best = s2.best;
-                out.bi = s2.bi;
-                out.pad0 = 0;
-                out.pad1 = 0;
-                a.partials[r + cta] = out;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int per = (a.rows + nth - 1) / nth;
+    const int r0 = tid * per;
+    uint32_t local = 0;
+    for (int k = 0; k < per; ++k) {
+        const int r = r0 + k;
+        if (r >= a.rows) break;
+        const uint8_t m = a.mask[r] ? 1 : 0;
+        mflag[r] = m;
+        const bool active = a.status[r / a.L] == EB_RUNNING;
+        const uint32_t w = active ? (uint32_t)a.nvec_row * (uint32_t)(m ? kWeightMasked : kWeightUnmasked) : 0u;
+        P[r] = w;
+        local += w;
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    uint32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t run = 0;
+        for (int w = 0; w < (nth + 31) / 32; ++w) {
+            const uint32_t t = scan[w];
+            scan[w] = run;
+            run += t;
+        }
+        P[a.rows] = run;
+    }
+    __syncthreads();
+    uint32_t base = scan[warp] + incl - local;
+    for (int k = 0; k < per; ++k) {
+        const int r = r0 + k;
+        if (r >= a.rows) break;
+        const uint32_t w = P[r];
+        P[r] = base;
+        base += w;
+    }
+    __syncthreads();
+}
+
+struct K1Smem {
+    static constexpr size_t ring = 0;
+    static constexpr size_t full = ring + (size_t)kStages * kStageBytes;
+    static constexpr size_t empty = full + (size_t)kStages * 8;
+    static constexpr size_t prefix = empty + (size_t)kStages * 8;
+    static constexpr size_t mflag = prefix + (size_t)(kMaxWeightedRows + 1) * 4;
+    static constexpr size_t red = (mflag + kMaxWeightedRows + 15) / 16 * 16;
+    static constexpr size_t scan = red + (size_t)kConsumerWarps * sizeof(RowState);
+    static constexpr size_t total = scan + 32 * 4;
+};
+
+__device__ __forceinline__ void write_partial(Partial *dst, const RowState &s, int flags)
+{
+    Partial out;
+    out.xm = s.xm;
+    out.S = s.S;
+    out.T2 = s.T2;
+    out.ai = s.ai;
+    out.best = s.best;
+    out.bi = s.bi;
+    out.flags = flags;
+    out.pad = 0;
+    *dst = out;
+}
+
+// Block reduction of the consumers' states and the partial write (consumer threads only).
+__device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, RowState *red, int row,
+                                                 int flags)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    warp_merge(st, a.c);
+    if (lane == 0) red[warp] = st;
+    consumer_sync();
+    if (warp == 0) {
+        RowState s2 = lane < kConsumerWarps ? red[lane] : empty_state();
+        warp_merge(s2, a.c);
+        if (lane == 0) write_partial(&a.partials[row + blockIdx.x], s2, flags);
+    }
+    consumer_sync();
+}
+
+// TMA path: rows start 16-byte aligned and hold whole 16-byte vectors.
+template <int KIND>
+__global__ void __launch_bounds__(kK1Threads, 1) k1_rowstats_tma(const K1Args a)
+{
+    using Tr = KindTraits<KIND>;
+    constexpr int VEC = Tr::VEC;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char *ring = smem + K1Smem::ring;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + K1Smem::full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + K1Smem::empty);
+    uint32_t *P = reinterpret_cast<uint32_t *>(smem + K1Smem::prefix);
+    uint8_t *mflag = smem + K1Smem::mflag;
+    RowState *red = reinterpret_cast<RowState *>(smem + K1Smem::red);
+    uint32_t *scan = reinterpret_cast<uint32_t *>(smem + K1Smem::scan);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.weighted) build_prefix(a, P, mflag, scan);
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (a.weighted && blockIdx.x == 0)
+        for (int r = tid; r <= a.rows; r += blockDim.x) a.prefix_out[r] = P[r];
+
+    const Partition part{P, a.nvec_row, a.rows, a.weighted};
+    SegmentCursor cur;
+    cur.begin(part, blockIdx.x, a.G);
+    int row;
+    long long j0, j1;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        uint32_t s = 0;
+        bool ok = true;
+        while (ok && cur.next(row, j0, j1)) {
+            if (!a.weighted && a.status[row / a.L] != EB_RUNNING) continue;
+            const char *src = static_cast<const char *>(a.logits) + (size_t)row * (size_t)a.row_bytes;
+            for (long long j = j0; j < j1; j += kVecPerStage) {
+                const uint32_t n = (uint32_t)min((long long)kVecPerStage, j1 - j);
+                const int slot = (int)(s % kStages);
+                if (s >= (uint32_t)kStages && !mbar_wait(&empty[slot], ((s / kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[slot], n * 16u);
+                bulk_g2s(ring + (size_t)slot * kStageBytes, src + j * 16, n * 16u, &full[slot]);
+                ++s;
             }
         }
-        __syncthreads();
+        // every issued copy has landed before this thread leaves
+        const uint32_t first = s > (uint32_t)kStages ? s - kStages : 0;
+        for (uint32_t q = first; q < s; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    uint32_t s = 0;
+    bool ok = true;
+    while (cur.next(row, j0, j1)) {
+        const int b = row / a.L;
+        if (!a.weighted && a.status[b] != EB_RUNNING) continue;
+        const uint32_t p = (uint32_t)(row - b * a.L);
+        const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
+        const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
+        RowState st = empty_state();
+        float nb = -st.xm * a.c;
+        float K = cand_scale(st.xm, st.best, a.c);
+        for (long long j = j0; ok && j < j1; j += kVecPerStage) {
+            const int n = (int)min((long long)kVecPerStage, j1 - j);
+            const int slot = (int)(s % kStages);
+            if (!mbar_wait(&full[slot], (s / kStages) & 1)) {
+                ok = false;
+                break;
+            }
+            const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (size_t)slot * kStageBytes);
+            if (masked) {
+#pragma unroll
+                for (int k = 0; k < kVecPerStage / kConsumers; ++k) {
+                    const int jj = tid + k * kConsumers;
+                    const bool valid = jj < n;
+                    float x[VEC];
+                    if (valid) Tr::unpack(stage[jj], x);
+                    consume_vec<VEC, true>(x, valid, j + jj, a, p, sw, st, nb, K);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kVecPerStage / kConsumers; ++k) {
+                    const int jj = tid + k * kConsumers;
+                    const bool valid = jj < n;
+                    float x[VEC];
+                    if (valid) Tr::unpack(stage[jj], x);
+                    consume_vec<VEC, false>(x, valid, j + jj, a, p, sw, st, nb, K);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            ++s;
+        }
+        reduce_and_store(st, a, red, row, ok ? 0 : kPartialTimeout);
+    }
+}
+
+// Scalar path (rows not 16-byte aligned): direct element loads, one entry per "vector".
+template <int KIND>
+__global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args a)
+{
+    __shared__ uint32_t P[kMaxWeightedRows + 1];
+    __shared__ uint8_t mflag[kMaxWeightedRows];
+    __shared__ RowState red[kConsumerWarps];
+    __shared__ uint32_t scan[32];
+    const int tid = threadIdx.x;
+    if (a.weighted) build_prefix(a, P, mflag, scan);
+    __syncthreads();
+    if (a.weighted && blockIdx.x == 0)
+        for (int r = tid; r <= a.rows; r += blockDim.x) a.prefix_out[r] = P[r];
+    const Partition part{P, a.nvec_row, a.rows, a.weighted};
+    SegmentCursor cur;
+    cur.begin(part, blockIdx.x, a.G);
+    int row;
+    long long j0, j1;
+    while (cur.next(row, j0, j1)) {
+        const int b = row / a.L;
+        if (!a.weighted && a.status[b] != EB_RUNNING) continue;
+        const uint32_t p = (uint32_t)(row - b * a.L);
+        const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
+        const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
+        const char *base = static_cast<const char *>(a.logits) + (size_t)row * (size_t)a.row_bytes;
+        RowState st = empty_state();
+        float nb = -st.xm * a.c;
+        float K = cand_scale(st.xm, st.best, a.c);
+        for (long long j = j0; j < j1; j += kConsumers) {
+            const long long v = j + tid;
+            const bool valid = v < j1;
+            float x[1] = {0.0f};
+            if (valid) {
+                if (KIND == kF32Scalar) x[0] = __ldg(reinterpret_cast<const float *>(base) + v);
+                else x[0] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(base) + v) << 16);
+            }
+            if (masked) consume_vec<1, true>(x, valid, v, a, p, sw, st, nb, K);
+            else consume_vec<1, false>(x, valid, v, a, p, sw, st, nb, K);
+        }
+        reduce_and_store(st, a, red, row, 0);
     }
 }
 
 // ------------------------------------------------------------------ selection kernel
 
-__device__ __forceinline__ long long range_start(long long c, long long N, int G)
+__device__ __forceinline__ unsigned long long k2_row_start(const K2Args &a, long long r)
 {
-    return c * N / G;
+    return a.weighted ? (unsigned long long)a.prefix[r]
+                      : (unsigned long long)r * (unsigned long long)a.nvec_row;
 }
 
-__device__ __forceinline__ int cta_of(long long i, long long N, int G)
-{
-    return (int)(((i + 1) * (long long)G - 1) / N);
-}
-
-__device__ double block_sum_double(double v, double *scratch)
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0) {
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += scratch[w];
-        scratch[32] = t;
-    }
-    __syncthreads();
-    return scratch[32];
+    return v;
 }
 
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        v = o < v ? o : v;
+    }
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long entropy_key(float H, int p)
+{
+    return ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
+}
+
+// One CTA per canvas.  Selection without a full sort: the positions with H <= bound
+// (fixed point) come first in (H, p) order, so only they need sorting, followed by the
+// lowest-entropy position above the bound, which is accepted iff every low one was and
+// their sum stays within the bound.  No later position can be accepted.
 __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
 {
-    __shared__ float Hs[kMaxL];
+    __shared__ unsigned long long Hq[kMaxL];     // entropies in 2^-40 nats
+    __shared__ float Hf[kMaxL];                  // entropies (binary32)
+    __shared__ unsigned long long keys[kMaxL];   // low-entropy candidates
+    __shared__ unsigned long long scanbuf[kMaxL];
     __shared__ int As[kMaxL];
     __shared__ int Ys[kMaxL];
-    __shared__ unsigned long long keys[kMaxL];
-    __shared__ double scan[kMaxL];
-    __shared__ double red[33];
-    __shared__ int counts[2];   // [0] committed this step, [1] masked before selection
+    __shared__ uint8_t Ms[kMaxL];                // masked before this step
+    __shared__ uint8_t Acc[kMaxL];               // accepted at this step
+    __shared__ unsigned long long red_sum[kK2Threads / 32];
+    __shared__ unsigned long long red_min[kK2Threads / 32];
+    __shared__ unsigned long long small_total;
+    __shared__ int n_masked, n_small, n_committed, bad_flags, all_small;
 
     const int b = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L;
-    if (a.status[b] != EB_RUNNING) return;   // CTA-uniform
-    const long long rowbase = (long long)b * L;
+    if (a.status[b] != EB_RUNNING) return;       // CTA-uniform
     if (tid == 0) {
-        counts[0] = 0;
-        counts[1] = 0;
+        n_masked = 0;
+        n_small = 0;
+        n_committed = 0;
+        bad_flags = 0;
+        all_small = 1;
+        small_total = 0;
     }
+    const long long rowbase = (long long)b * L;
+    const unsigned long long W = k2_row_start(a, a.rows);
+    const unsigned long long G = (unsigned long long)a.G;
+    __syncthreads();
 
-    // 1. merge the per-CTA partials of every row in ascending CTA order (deterministic)
-    int bad = 0, unstable = 0, my_masked = 0;
-    double hsum = 0.0;
+    // 1. merge each row's partials (ascending CTA) -> H, A, Y
+    unsigned long long my_sum = 0, my_bigmin = ~0ull;
+    int my_unstable = 0, my_bad = 0, my_masked = 0, my_small = 0;
     for (int p = tid; p < L; p += blockDim.x) {
         const long long r = rowbase + p;
-        const long long ifirst = r * a.nvec_row;
-        const long long ilast = ifirst + a.nvec_row - 1;
-        const int c0 = cta_of(ifirst, a.N, a.G);
-        const int c1 = cta_of(ilast, a.N, a.G);
-        RowState st{kEmptyMax, 0.0f, 0.0f, 0x7FFFFFFF, -INFINITY, -1};
-        for (int cc = c0; cc <= c1; ++cc) {
-            if (range_start(cc, a.N, a.G) >= range_start(cc + 1, a.N, a.G)) continue;
-            const Partial q = a.partials[r + cc];
-            merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
+        const unsigned long long w0 = k2_row_start(a, r), w1 = k2_row_start(a, r + 1);
+        RowState st = empty_state();
+        int flags = 0;
+        if (w1 > w0) {
+            const int c0 = (int)(((w0 + 1) * G - 1) / W);
+            const int c1 = (int)((w1 * G - 1) / W);
+            for (int c = c0; c <= c1; ++c) {
+                if ((unsigned long long)c * W / G >= (unsigned long long)(c + 1) * W / G) continue;
+                const Partial q = a.partials[r + c];
+                merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
+                flags |= q.flags;
+            }
         }
         float H = kLn2 * (log2f(st.S) - st.T2 / st.S);
-        if (H < 0.0f) H = 0.0f;            // rounding below zero (NaN passes through)
-        H = H + 0.0f;                      // -0 -> +0 so the key bits sort correctly
-        bad |= (!isfinite(H) || !isfinite(st.xm)) ? 1 : 0;
-        const bool masked = a.mask[r] != 0;
-        my_masked += masked ? 1 : 0;
+        if (H < 0.0f) H = 0.0f;                  // rounding below zero (NaN passes through)
+        H = H + 0.0f;                            // -0 -> +0 so the key bits order correctly
+        const bool bad = !isfinite(H) || !isfinite(st.xm) || flags != 0;
+        if (bad) my_bad |= flags ? 2 : 1;
+        const uint8_t m = a.mask[r] ? 1 : 0;
         const int A = st.ai;
-        const int Y = masked ? st.bi : -1;
-        Hs[p] = H;
+        const int Y = m ? st.bi : -1;
+        const unsigned long long hq = bad ? 0ull : (unsigned long long)__float2ull_rn(H * 1099511627776.0f);
+        Hq[p] = hq;
+        Hf[p] = H;
         As[p] = A;
         Ys[p] = Y;
+        Ms[p] = m;
+        Acc[p] = 0;
         a.entropy[r] = H;
         a.argmax[r] = A;
         a.sampled[r] = Y;
-        a.selected[r] = 0;
-        hsum += (double)H;
-        unstable |= (a.prev_argmax[r] != A) ? 1 : 0;
+        my_sum += hq;
+        my_unstable |= (a.prev_argmax[r] != A) ? 1 : 0;
+        if (m) {
+            ++my_masked;
+            if ((long long)hq <= a.bound_q) {
+                ++my_small;
+            } else {
+                const unsigned long long key = entropy_key(H, p);
+                my_bigmin = key < my_bigmin ? key : my_bigmin;
+            }
+        }
     }
-    if (__syncthreads_or(bad)) {
+    const unsigned long long ws = warp_sum_u64(my_sum);
+    const unsigned long long wm = warp_min_u64(my_bigmin);
+    if (lane == 0) {
+        red_sum[warp] = ws;
+        red_min[warp] = wm;
+    }
+    if (my_masked) atomicAdd(&n_masked, my_masked);
+    if (my_small) atomicAdd(&n_small, my_small);
+    if (my_bad) atomicOr(&bad_flags, my_bad);
+    const bool stable = __syncthreads_or(my_unstable) == 0;
+    unsigned long long sumq = 0, bigmin = ~0ull;
+    for (int w = 0; w < kK2Threads / 32; ++w) {
+        sumq += red_sum[w];
+        bigmin = red_min[w] < bigmin ? red_min[w] : bigmin;
+    }
+    const int nm = n_masked, ns = n_small;
+    const float mean = (float)((double)sumq / 1099511627776.0 / (double)L);
+    if (bad_flags) {
         if (tid == 0) {
-            a.status[b] = EB_STATUS_NONFINITE;
+            a.status[b] = EB_STATUS_NONFINITE | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
             if (a.steps_taken) a.steps_taken[b] = a.step + 1;
             if (a.committed) a.committed[b] = 0;
             if (a.mean_entropy) a.mean_entropy[b] = NAN;
         }
+        for (int p = tid; p < L; p += blockDim.x) a.selected[rowbase + p] = 0;
         return;
     }
-    if (my_masked) atomicAdd(&counts[1], my_masked);
-    const double mean = block_sum_double(hsum, red) / (double)L;   // has barriers
-    const bool stable = __syncthreads_or(unstable) == 0;
-    const bool stop = a.step >= 1 && stable && mean < (double)a.stop_entropy;
-    const int nm = counts[1];
+    const bool stop = a.step >= 1 && stable && (long long)sumq < a.stop_q;
 
-    int my_commit = 0;
-    int new_status = EB_RUNNING;
     if (stop) {
         // adaptive stop: every still-masked position takes its argmax
+        for (int p = tid; p < L; p += blockDim.x) Acc[p] = Ms[p];
+    } else if (nm > 0) {
+        // 2. gather the low-entropy candidates
+        if (tid == 0) n_small = 0;
+        __syncthreads();
         for (int p = tid; p < L; p += blockDim.x) {
-            const long long r = rowbase + p;
-            if (a.mask[r]) {
-                a.tokens[r] = As[p];
-                a.mask[r] = 0;
-                a.selected[r] = 1;
-                ++my_commit;
+            if (Ms[p] && (long long)Hq[p] <= a.bound_q) {
+                const int i = atomicAdd(&n_small, 1);
+                keys[i] = entropy_key(Hf[p], p);
             }
         }
-        new_status = EB_STOP_ADAPTIVE;
-    } else {
-        // 2. bitonic sort of (H bits << 32 | p) for masked p; unmasked keys sort last
-        int n2 = 1;
-        while (n2 < L) n2 <<= 1;
-        for (int i = tid; i < n2; i += blockDim.x) {
-            unsigned long long k = ~0ull;
-            if (i < L && a.mask[rowbase + i])
-                k = ((unsigned long long)__float_as_uint(Hs[i]) << 32) | (unsigned)i;
-            keys[i] = k;
-        }
         __syncthreads();
-        for (int k = 2; k <= n2; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < n2; i += blockDim.x) {
-                    const int ixj = i ^ j;
-                    if (ixj > i) {
-                        const unsigned long long x = keys[i], y = keys[ixj];
-                        const bool asc = (i & k) == 0;
-                        if ((x > y) == asc) {
-                            keys[i] = y;
-                            keys[ixj] = x;
-                        }
+        if (ns <= 32) {
+            if (warp == 0) {
+                unsigned long long k = lane < ns ? keys[lane] : ~0ull;
+                // bitonic sort of 32 keys across the warp, ascending
+#pragma unroll
+                for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, k, stride);
+                        const bool up = (lane & size) == 0;
+                        const bool lower = (lane & stride) == 0;
+                        const unsigned long long lo = o < k ? o : k, hi = o < k ? k : o;
+                        k = (lower == up) ? lo : hi;
                     }
                 }
-                __syncthreads();
-            }
-        }
-        // 3. inclusive prefix sums of the sorted entropies in binary64 (Hillis-Steele)
-        for (int i = tid; i < n2; i += blockDim.x)
-            scan[i] = (i < nm) ? (double)__uint_as_float((unsigned)(keys[i] >> 32)) : 0.0;
-        __syncthreads();
-        for (int off = 1; off < n2; off <<= 1) {
-            double add[kMaxL / kK2Threads];
-            int q = 0;
-            for (int i = tid; i < n2; i += blockDim.x, ++q) add[q] = (i >= off) ? scan[i - off] : 0.0;
-            __syncthreads();
-            q = 0;
-            for (int i = tid; i < n2; i += blockDim.x, ++q) scan[i] += add[q];
-            __syncthreads();
-        }
-        // 4. accept sorted index i iff i == 0 or sum_{j<i} H_(j) <= bound; commit Y
-        int my_left = 0;
-        for (int i = tid; i < nm; i += blockDim.x) {
-            const double before = (i == 0) ? 0.0 : scan[i - 1];
-            const int pos = (int)(keys[i] & 0xFFFFFFFFu);
-            const long long r = rowbase + pos;
-            if (i == 0 || before <= (double)a.bound) {
-                a.tokens[r] = Ys[pos];
-                a.mask[r] = 0;
-                a.selected[r] = 1;
-                ++my_commit;
-            } else {
-                ++my_left;
-            }
-        }
-        const bool any_left = __syncthreads_or(my_left) != 0;
-        if (!any_left) {
-            new_status = EB_STOP_COMPLETE;
-        } else if (a.step >= a.max_steps - 1) {
-            // step cap: the rest take their argmax (mask writes above are visible: barrier)
-            for (int p = tid; p < L; p += blockDim.x) {
-                const long long r = rowbase + p;
-                if (a.mask[r]) {
-                    a.tokens[r] = As[p];
-                    a.mask[r] = 0;
-                    a.selected[r] = 1;
-                    ++my_commit;
+                const int pos = (int)(k & 0xFFFFFFFFu);
+                const unsigned long long h = lane < ns ? Hq[pos] : 0ull;
+                unsigned long long incl = h;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                const unsigned long long excl = incl - h;
+                const bool acc = lane < ns && (lane == 0 || (long long)excl <= a.bound_q);
+                if (acc) Acc[pos] = 1;
+                const unsigned ok_mask = __ballot_sync(0xFFFFFFFFu, acc || lane >= ns);
+                const unsigned long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                if (lane == 0) {
+                    all_small = ok_mask == 0xFFFFFFFFu ? 1 : 0;
+                    small_total = tot;
                 }
             }
-            new_status = EB_STOP_CAP;
+        } else {
+            // general path: bitonic sort of the ns candidates in shared memory
+            int n2 = 1;
+            while (n2 < ns) n2 <<= 1;
+            for (int i = ns + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+            __syncthreads();
+            for (int size = 2; size <= n2; size <<= 1) {
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    for (int i = tid; i < n2; i += blockDim.x) {
+                        const int ixj = i ^ stride;
+                        if (ixj > i) {
+                            const unsigned long long x = keys[i], y = keys[ixj];
+                            const bool up = (i & size) == 0;
+                            if ((x > y) == up) {
+                                keys[i] = y;
+                                keys[ixj] = x;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            // inclusive scan of the sorted fixed-point entropies (Hillis-Steele)
+            for (int i = tid; i < n2; i += blockDim.x)
+                scanbuf[i] = i < ns ? Hq[(int)(keys[i] & 0xFFFFFFFFu)] : 0ull;
+            __syncthreads();
+            for (int off = 1; off < n2; off <<= 1) {
+                unsigned long long add[kMaxL / kK2Threads];
+                int q = 0;
+                for (int i = tid; i < n2; i += blockDim.x, ++q) add[q] = i >= off ? scanbuf[i - off] : 0ull;
+                __syncthreads();
+                q = 0;
+                for (int i = tid; i < n2; i += blockDim.x, ++q) scanbuf[i] += add[q];
+                __syncthreads();
+            }
+            int my_rej = 0;
+            for (int i = tid; i < ns; i += blockDim.x) {
+                const unsigned long long excl = i == 0 ? 0ull : scanbuf[i - 1];
+                if (i == 0 || (long long)excl <= a.bound_q) Acc[(int)(keys[i] & 0xFFFFFFFFu)] = 1;
+                else my_rej = 1;
+            }
+            if (my_rej) all_small = 0;
+            if (tid == 0) small_total = scanbuf[ns - 1];
+        }
+        __syncthreads();
+        // sorted index ns: the lowest-entropy position above the bound
+        if (tid == 0 && bigmin != ~0ull) {
+            if (ns == 0 || (all_small && (long long)small_total <= a.bound_q))
+                Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
         }
     }
-    for (int p = tid; p < L; p += blockDim.x) a.prev_argmax[rowbase + p] = As[p];
-    if (my_commit) atomicAdd(&counts[0], my_commit);
+    __syncthreads();
+
+    // 3. commit, re-mask, complete / cap
+    int my_left = 0;
+    for (int p = tid; p < L; p += blockDim.x) my_left |= (Ms[p] && !Acc[p]) ? 1 : 0;
+    const bool any_left = __syncthreads_or(my_left) != 0;
+    int new_status = EB_RUNNING;
+    if (stop) new_status = EB_STOP_ADAPTIVE;
+    else if (!any_left) new_status = EB_STOP_COMPLETE;
+    else if (a.step >= a.max_steps - 1) new_status = EB_STOP_CAP;
+    int my_commit = 0;
+    for (int p = tid; p < L; p += blockDim.x) {
+        const long long r = rowbase + p;
+        uint8_t sel = 0;
+        if (Acc[p]) {
+            a.tokens[r] = stop ? As[p] : Ys[p];
+            a.mask[r] = 0;
+            sel = 1;
+        } else if (Ms[p] && new_status == EB_STOP_CAP) {
+            a.tokens[r] = As[p];
+            a.mask[r] = 0;
+            sel = 1;
+        }
+        my_commit += sel;
+        a.selected[r] = sel;
+        a.prev_argmax[r] = As[p];
+    }
+    if (my_commit) atomicAdd(&n_committed, my_commit);
     __syncthreads();
     if (tid == 0) {
-        const int cnt = counts[0];
+        const int committed = n_committed;
         if (new_status != EB_RUNNING) {
             a.status[b] = new_status;
             if (a.steps_taken) a.steps_taken[b] = a.step + 1;
         }
-        if (a.committed) a.committed[b] = cnt;
-        if (a.mean_entropy) a.mean_entropy[b] = (float)mean;
-        if (a.committed_hist) a.committed_hist[(long long)b * a.max_steps + a.step] = cnt;
-        if (a.mean_hist) a.mean_hist[(long long)b * a.max_steps + a.step] = (float)mean;
+        if (a.committed) a.committed[b] = committed;
+        if (a.mean_entropy) a.mean_entropy[b] = mean;
+        if (a.committed_hist) a.committed_hist[(long long)b * a.max_steps + a.step] = committed;
+        if (a.mean_hist) a.mean_hist[(long long)b * a.max_steps + a.step] = mean;
     }
 }
 
@@ -670,22 +683,21 @@ eb_status ok()
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Per-device launch geometry of the row-statistics kernels, filled once per device.
+// Per-device launch geometry, filled once per device.
 struct DeviceGeometry {
     std::atomic<int> ready{0};
-    int grid[4] = {0, 0, 0, 0};   // SMs x resident CTAs for each element kind
+    int grid[4] = {0, 0, 0, 0};   // CTAs of k1 for each element kind
 };
 DeviceGeometry g_geometry[64];
 
-template <int KIND>
-int resident_grid(int nsm)
+template <typename K>
+int resident_ctas(K kernel, int threads, size_t smem, int nsm)
 {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ebk::k1_rowstats<KIND>,
-                                                      ebk::kK1Threads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
-    long long g = (long long)nsm * per_sm;
+    const long long g = (long long)nsm * per_sm;
     return (int)(g > ebk::kMaxGrid ? ebk::kMaxGrid : g);
 }
 
@@ -696,12 +708,23 @@ eb_status geometry(int *grid_out, int kind)
     if (dev < 0 || dev >= 64) return fail(EB_ERR_UNSUPPORTED, "device index %d >= 64", dev);
     DeviceGeometry &g = g_geometry[dev];
     if (g.ready.load(std::memory_order_acquire) == 0) {
-        int nsm = 0;
-        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        int nsm = 0, smem_optin = 0;
+        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return fail(EB_ERR_CUDA, "cudaDeviceGetAttribute failed");
-        int grid[4] = {resident_grid<ebk::kF32Vec>(nsm), resident_grid<ebk::kBF16Vec>(nsm),
-                       resident_grid<ebk::kF32Scalar>(nsm), resident_grid<ebk::kBF16Scalar>(nsm)};
-        for (int i = 0; i < 4; ++i) g.grid[i] = grid[i];
+        const size_t smem = ebk::K1Smem::total;
+        if ((size_t)smem_optin < smem)
+            return fail(EB_ERR_UNSUPPORTED, "device offers %d B of shared memory per block, need %zu",
+                        smem_optin, smem);
+        if (cudaFuncSetAttribute(ebk::k1_rowstats_tma<ebk::kF32Vec>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(ebk::k1_rowstats_tma<ebk::kBF16Vec>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
+        g.grid[ebk::kF32Vec] = resident_ctas(ebk::k1_rowstats_tma<ebk::kF32Vec>, ebk::kK1Threads, smem, nsm);
+        g.grid[ebk::kBF16Vec] = resident_ctas(ebk::k1_rowstats_tma<ebk::kBF16Vec>, ebk::kK1Threads, smem, nsm);
+        g.grid[ebk::kF32Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kF32Scalar>, ebk::kConsumers, 0, nsm);
+        g.grid[ebk::kBF16Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kBF16Scalar>, ebk::kConsumers, 0, nsm);
         g.ready.store(1, std::memory_order_release);
     }
     *grid_out = g.grid[kind];
@@ -727,10 +750,9 @@ float schedule_temperature(const eb_params *p, int step)
     return p->t_start + (p->t_end - p->t_start) * (float)step / (float)(p->max_steps - 1);
 }
 
-size_t partial_bytes(long long rows)
-{
-    return align256((size_t)(rows + ebk::kMaxGrid) * sizeof(ebk::Partial));
-}
+// Workspace layout: [partials (rows + kMaxGrid) x 32 B][weight prefix (rows + 1) x 4 B].
+size_t partial_bytes(long long rows) { return align256((size_t)(rows + ebk::kMaxGrid) * sizeof(ebk::Partial)); }
+size_t prefix_bytes(long long rows) { return align256((size_t)(rows + 1) * sizeof(uint32_t)); }
 
 struct StepBuffers {
     uint8_t *mask;
@@ -753,8 +775,9 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
     if (!(params->t_start > 0.0f) || !(params->t_end > 0.0f) || !std::isfinite(params->t_start) ||
         !std::isfinite(params->t_end))
         return fail(EB_ERR_INVALID, "temperatures must be finite and > 0");
-    if (!std::isfinite(params->entropy_bound) || !std::isfinite(params->stop_entropy))
-        return fail(EB_ERR_INVALID, "entropy_bound / stop_entropy must be finite");
+    if (!std::isfinite(params->entropy_bound) || !std::isfinite(params->stop_entropy) ||
+        std::fabs(params->entropy_bound) > 1.0e6f || std::fabs(params->stop_entropy) > 1.0e6f)
+        return fail(EB_ERR_INVALID, "entropy_bound / stop_entropy must be finite and below 1e6");
     if (B < 0) return fail(EB_ERR_INVALID, "B must be >= 0 (got %d)", B);
     if (L < 1 || L > ebk::kMaxL) return fail(EB_ERR_INVALID, "L must be in [1, %d] (got %d)", ebk::kMaxL, L);
     if (V < 1) return fail(EB_ERR_INVALID, "V must be >= 1 (got %d)", V);
@@ -765,7 +788,7 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
         !sb.sampled || !sb.selected)
         return fail(EB_ERR_INVALID, "a required state / output pointer is NULL");
     const long long rows = (long long)B * L;
-    if (rows > (1ll << 31) - ebk::kMaxGrid) return fail(EB_ERR_UNSUPPORTED, "B*L too large");
+    if (rows > (1ll << 31) - 1 - ebk::kMaxGrid) return fail(EB_ERR_UNSUPPORTED, "B*L too large");
     if (!d_ws) return fail(EB_ERR_WORKSPACE, "workspace is NULL");
     if (((uintptr_t)d_ws & 255) != 0) return fail(EB_ERR_WORKSPACE, "workspace not 256-byte aligned");
     if (ws_bytes < eb_workspace_bytes(B, L, V, dtype))
@@ -792,18 +815,26 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     const long long nvec_row = V / vec;
     const long long N = rows * nvec_row;
     if (N > (1ll << 48)) return fail(EB_ERR_UNSUPPORTED, "B*L*V too large");
+    const bool weighted = rows <= ebk::kMaxWeightedRows &&
+                          (unsigned long long)N * ebk::kWeightMasked < (1ull << 32);
     const int G = (int)(N < gmax ? N : gmax);
+    char *ws = static_cast<char *>(d_ws);
+    ebk::Partial *partials = reinterpret_cast<ebk::Partial *>(ws);
+    uint32_t *prefix = reinterpret_cast<uint32_t *>(ws + partial_bytes(rows));
 
     ebk::K1Args a1;
     a1.logits = d_logits;
     a1.mask = sb.mask;
     a1.status = sb.status;
-    a1.partials = static_cast<ebk::Partial *>(d_ws);
+    a1.partials = partials;
+    a1.prefix_out = prefix;
     a1.nvec_row = nvec_row;
-    a1.N = N;
+    a1.row_bytes = (long long)V * (long long)esize;
+    a1.rows = (int)rows;
     a1.L = L;
     a1.G = G;
     a1.step = step;
+    a1.weighted = weighted ? 1 : 0;
     a1.c = ebk::kLog2e / T;
     a1.invT = 1.0f / T;
     a1.keys = round_keys(params->seed);
@@ -811,11 +842,12 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     g_profile_begin = g_profile_end = nullptr;
     if (prof_begin && cudaEventRecord(prof_begin, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
+    const size_t smem = ebk::K1Smem::total;
     switch (kind) {
-    case ebk::kF32Vec: ebk::k1_rowstats<ebk::kF32Vec><<<G, ebk::kK1Threads, 0, stream>>>(a1); break;
-    case ebk::kBF16Vec: ebk::k1_rowstats<ebk::kBF16Vec><<<G, ebk::kK1Threads, 0, stream>>>(a1); break;
-    case ebk::kF32Scalar: ebk::k1_rowstats<ebk::kF32Scalar><<<G, ebk::kK1Threads, 0, stream>>>(a1); break;
-    default: ebk::k1_rowstats<ebk::kBF16Scalar><<<G, ebk::kK1Threads, 0, stream>>>(a1); break;
+    case ebk::kF32Vec: ebk::k1_rowstats_tma<ebk::kF32Vec><<<G, ebk::kK1Threads, smem, stream>>>(a1); break;
+    case ebk::kBF16Vec: ebk::k1_rowstats_tma<ebk::kBF16Vec><<<G, ebk::kK1Threads, smem, stream>>>(a1); break;
+    case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    default: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
@@ -823,7 +855,8 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
 
     ebk::K2Args a2;
-    a2.partials = static_cast<const ebk::Partial *>(d_ws);
+    a2.partials = partials;
+    a2.prefix = prefix;
     a2.mask = sb.mask;
     a2.tokens = sb.tokens;
     a2.prev_argmax = sb.prev_argmax;
@@ -838,14 +871,16 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a2.committed_hist = sb.committed_hist;
     a2.mean_hist = sb.mean_hist;
     a2.nvec_row = nvec_row;
-    a2.N = N;
+    a2.rows = (int)rows;
     a2.L = L;
     a2.G = G;
     a2.step = step;
     a2.max_steps = params->max_steps;
+    a2.weighted = a1.weighted;
     a2.c = a1.c;
-    a2.bound = params->entropy_bound;
-    a2.stop_entropy = params->stop_entropy;
+    // fixed point, 2^-40 nats: accept while prefix <= floor(bound), stop while sum < ceil(stop L)
+    a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
+    a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
     ebk::k2_select<<<B, ebk::kK2Threads, 0, stream>>>(a2);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "selection launch: %s", cudaGetErrorString(e));
@@ -880,7 +915,7 @@ size_t eb_workspace_bytes(int B, int L, int V, eb_dtype dtype)
     (void)V;
     (void)dtype;
     if (B < 0 || L < 1) return 0;
-    return partial_bytes((long long)B * L);
+    return partial_bytes((long long)B * L) + prefix_bytes((long long)B * L);
 }
 
 eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype dtype,

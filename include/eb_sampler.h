@@ -30,8 +30,9 @@
  *     work is enqueued asynchronously on it;
  *   - argument errors return before any launch and leave every buffer untouched;
  *     eb_last_error() then holds a one-line description (thread-local);
- *   - device-detected problems never trap: a canvas whose logits hold NaN or +Inf gets
- *     EB_STATUS_NONFINITE or-ed into its status word and is halted;
+ *   - logits must be finite with |x| < 1e37 (exclude a token with a large negative finite
+ *     value such as -1e30); device-detected problems never trap: a canvas whose logits hold
+ *     NaN or +-Inf gets EB_STATUS_NONFINITE in its status word and is halted;
  *   - layouts are row-major: logits [B, L, V] with V contiguous; per-position arrays
  *     [B, L]; per-canvas arrays [B];
  *   - tokens use -1 for MASK.
@@ -62,7 +63,8 @@ typedef enum { EB_F32 = 0, EB_BF16 = 1 } eb_dtype;
 #define EB_STOP_ADAPTIVE 1       /* mean entropy < stop_entropy and argmax stable */
 #define EB_STOP_COMPLETE 2       /* every position committed by selection */
 #define EB_STOP_CAP 3            /* the last step (max_steps - 1) was reached */
-#define EB_STATUS_NONFINITE 0x100 /* or-ed in: NaN / +Inf logits seen; canvas halted */
+#define EB_STATUS_NONFINITE 0x100 /* or-ed in: NaN / +-Inf logits seen; canvas halted */
+#define EB_STATUS_TIMEOUT 0x200   /* or-ed in: a bounded device wait gave up; canvas halted */
 
 typedef struct {
     int32_t max_steps;     /* 48 */

@@ -131,13 +131,16 @@ def test_step_parity_single_step_workload_full_size(seed):
 
 # ------------------------------------------------------------------ the loop
 
-def _lockstep(cfg, params_kw=None, mask=None, sampled_rows=None, max_compare_steps=None):
-    """Run eb_sampler_step step by step next to the oracle; return (reports, gpu history)."""
+def _lockstep(cfg, params_kw=None, mask=None):
+    """Run eb_sampler_step step by step next to the oracle; compare every step until a
+    counted tie lets the trajectories part, then keep running the GPU alone.  Returns
+    (report, GPU state after every step, canvas)."""
     gp, op = params_pair(seed=cfg.seeds[0], **(params_kw or {}))
     c = eb.Canvas(cfg.B, cfg.L, cfg.V, _dtype(cfg), mask=mask, max_steps=gp.max_steps)
     ost = oracle.State.fresh(cfg.B, cfg.L, mask)
     rep = Report()
     hist = []
+    parted = set()
     for s in range(gp.max_steps):
         st_before = c.status.cpu().numpy()
         if not (st_before == eb.EB_RUNNING).any():
@@ -146,16 +149,14 @@ def _lockstep(cfg, params_kw=None, mask=None, sampled_rows=None, max_compare_ste
         c.step(gp, dev, s, 0.0)
         g = host_state(c)
         hist.append(g)
-        if max_compare_steps is not None and s >= max_compare_steps:
-            continue
         running = ost.status == oracle.RUNNING
-        if not np.array_equal(running, st_before == eb.EB_RUNNING):
-            break      # trajectories parted after a counted tie
         x = cfg.logits(s)
         res = oracle.step(x, ost, s, op)
-        tied = compare_step(g, res, ost, running, rep, ctx=f"step {s}")
-        if tied:
-            break
+        # canvases whose trajectories parted after a counted tie are no longer compared
+        view = running & (st_before == eb.EB_RUNNING)
+        for b in parted:
+            view[b] = False
+        parted |= compare_step(g, res, ost, view, rep, ctx=f"step {s}")
     return rep, hist, c
 
 
@@ -283,7 +284,7 @@ def test_stopped_canvases_untouched():
 
 
 def test_nonfinite_logits_set_status_bit():
-    for bad in (np.nan, np.inf):
+    for bad in (np.nan, np.inf, -np.inf):
         x = np.zeros((2, 8, 64), np.float32)
         x[1, 3, 5] = bad
         c = eb.Canvas(2, 8, 64, eb.EB_F32)
@@ -292,15 +293,20 @@ def test_nonfinite_logits_set_status_bit():
         g = host_state(c)
         assert g["status"][1] & eb.EB_STATUS_NONFINITE
         assert g["status"][0] == eb.EB_RUNNING
+        assert (g["mask"][1] == 1).all() and (g["tokens"][1] == -1).all()
 
 
-def test_minus_inf_logits_k_point_entropy():
-    # k equal top logits and the rest -inf: H = ln k, sample among the k, argmax = first
-    x = np.full((1, 4, 4096), -np.inf, np.float32)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_excluded_tokens_k_point_entropy(dtype):
+    # k equal top logits and the rest -1e30 (excluded): H = ln k, the sample is one of the
+    # k, the argmax the first of them -- the oracle's k-point closed form with -inf
+    x = np.full((1, 4, 4096), -1.0e30, np.float32)
     tops = {0: [5], 1: [7, 900], 2: [1, 2, 3], 3: list(range(100, 4096, 64))}
     for p, t in tops.items():
         x[0, p, t] = 1.5
-    c = eb.Canvas(1, 4, 4096, eb.EB_F32)
+    if dtype == "bf16":
+        x = eb_synth.to_bf16_bits(x)
+    c = eb.Canvas(1, 4, 4096, eb.EB_BF16 if dtype == "bf16" else eb.EB_F32)
     gp, _ = params_pair(entropy_bound=-1.0)
     c.step(gp, to_device_logits(x), 0, 0.0)
     g = host_state(c)

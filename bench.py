@@ -128,66 +128,83 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running."""
+    """Samples SM clock, power and clock-event reasons with nvidia-smi (200 ms period) while
+    the timed region runs."""
 
-    REASONS = {
-        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
-        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
-        "display_clock_setting": 0x100,
-    }
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMED = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
-        self.samples = []
-        self.max_mhz = None
-        self.ok = False
-        self._stop = threading.Event()
-        self.period = period_s
+    def __init__(self, device_index: int, log_path: str | None = None):
+        import tempfile
+        self.device_index = device_index
+        self.log_path = log_path or tempfile.mktemp(prefix="eb_clocks_", suffix=".csv")
+        self.proc = None
+        self.rows = []
+
+    def _target(self):
         try:
-            import pynvml
             import torch
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-            self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            pr = torch.cuda.get_device_properties(self.device_index)
+            return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
         except Exception:
-            self._nv = None
-
-    def _run(self):
-        nv = self._nv
-        while not self._stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
-                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                self.samples.append((mhz, reasons))
-            except Exception:
-                pass
-            time.sleep(self.period)
+            return str(self.device_index)
 
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        import subprocess
+        try:
+            self._f = open(self.log_path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._target(), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self._f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
-        self._stop.set()
-        if self.ok:
-            self._t.join()
+        self.t1 = time.time()
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._f.close()
+            import datetime
+            for line in open(self.log_path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None
+                # keep the samples taken while the timed region ran (one period of slack)
+                if ts is None or self.t0 - 0.2 <= ts <= self.t1 + 0.2:
+                    self.rows.append(f)
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
-        mhz = statistics.median(s[0] for s in self.samples)
-        bits = 0
-        for _, r in self.samples:
-            bits |= r
-        names = [k for k, v in self.REASONS.items() if bits & v and k != "gpu_idle"]
-        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples)}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        mhz = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        reasons = set()
+        for r in self.rows:
+            for name, val in zip(self.NAMED, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in self.rows) if self.rows else None}
 
 
 # ------------------------------------------------------------------ the workload

@@ -61,6 +61,7 @@ constexpr float kOneMinusHalfUlp = 0.99999994039535522f;  // 1 - 2^-24
 constexpr uint32_t kStreamGumbel = 1u;
 
 constexpr int kPartialTimeout = 1;                  // Partial::flags: a wait gave up
+constexpr int kPartialNonfinite = 2;                // Partial::flags: NaN reached the sums
 
 // Philox4x32-10 round keys (k0 + r 0x9E3779B9, k1 + r 0xBB67AE85), r = 0..9, precomputed
 // on the host; as a kernel parameter every key xor reads the constant bank.
@@ -193,8 +194,11 @@ __device__ __forceinline__ void merge_state(RowState &a, float xm, float S, floa
     const float da = (a.xm - m) * c;
     const float db = (xm - m) * c;
     const float sa = ex2(da), sb = ex2(db);
-    const float T2n = sa * fmaf(da, a.S, a.T2) + sb * fmaf(db, S, T2);
-    const float Sn = a.S * sa + S * sb;
+    // a side whose weight underflows to 0 contributes nothing, even if its sums overflowed
+    // (a slice holding only excluded entries far below the row maximum)
+    const float T2n = (sa == 0.0f ? 0.0f : sa * fmaf(da, a.S, a.T2)) +
+                      (sb == 0.0f ? 0.0f : sb * fmaf(db, S, T2));
+    const float Sn = (sa == 0.0f ? 0.0f : a.S * sa) + (sb == 0.0f ? 0.0f : S * sb);
     int ain;
     if (a.xm > xm) ain = a.ai;
     else if (xm > a.xm) ain = ai;

@@ -82,8 +82,8 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
             // new running max: rescale the sums and take its first index as the argmax
             const float d = (st.xm - vmax) * a.c;
             const float sc = ex2(d);
-            st.T2 = sc * fmaf(d, st.S, st.T2);
-            st.S *= sc;
+            st.T2 = sc == 0.0f ? 0.0f : sc * fmaf(d, st.S, st.T2);
+            st.S = sc == 0.0f ? 0.0f : st.S * sc;
             int j0 = VEC - 1;
 #pragma unroll
             for (int j = VEC - 1; j >= 0; --j)
@@ -206,17 +206,23 @@ __device__ __forceinline__ void write_partial(Partial *dst, const RowState &s, i
 }
 
 // Block reduction of the consumers' states and the partial write (consumer threads only).
-__device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, RowState *red, int row,
-                                                 int flags)
+// A NaN in any thread's sums is recorded before the merge can scale it away.
+__device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, RowState *red,
+                                                 uint32_t *redflag, int row, int flags)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
     warp_merge(st, a.c);
-    if (lane == 0) red[warp] = st;
+    if (lane == 0) {
+        red[warp] = st;
+        redflag[warp] = nan_here ? (uint32_t)kPartialNonfinite : 0u;
+    }
     consumer_sync();
     if (warp == 0) {
         RowState s2 = lane < kConsumerWarps ? red[lane] : empty_state();
+        const uint32_t nf = __reduce_or_sync(0xFFFFFFFFu, lane < kConsumerWarps ? redflag[lane] : 0u);
         warp_merge(s2, a.c);
-        if (lane == 0) write_partial(&a.partials[row + blockIdx.x], s2, flags);
+        if (lane == 0) write_partial(&a.partials[row + blockIdx.x], s2, flags | (int)nf);
     }
     consumer_sync();
 }
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(kK1Threads, 1) k1_rowstats_tma(const K1Args a)
             if (lane == 0) mbar_arrive(&empty[slot]);
             ++s;
         }
-        reduce_and_store(st, a, red, row, ok ? 0 : kPartialTimeout);
+        reduce_and_store(st, a, red, scan, row, ok ? 0 : kPartialTimeout);
     }
 }
 
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
             if (masked) consume_vec<1, true>(x, valid, v, a, p, sw, st, nb, K);
             else consume_vec<1, false>(x, valid, v, a, p, sw, st, nb, K);
         }
-        reduce_and_store(st, a, red, row, 0);
+        reduce_and_store(st, a, red, scan, row, 0);
     }
 }
 
@@ -458,8 +464,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         float H = kLn2 * (log2f(st.S) - st.T2 / st.S);
         if (H < 0.0f) H = 0.0f;                  // rounding below zero (NaN passes through)
         H = H + 0.0f;                            // -0 -> +0 so the key bits order correctly
-        const bool bad = !isfinite(H) || !isfinite(st.xm) || flags != 0;
-        if (bad) my_bad |= flags ? 2 : 1;
+        if (!isfinite(H) || !isfinite(st.xm) || (flags & kPartialNonfinite)) my_bad |= 1;
+        if (flags & kPartialTimeout) my_bad |= 2;
+        const bool bad = my_bad != 0;
         const uint8_t m = a.mask[r] ? 1 : 0;
         const int A = st.ai;
         const int Y = m ? st.bi : -1;
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     const float mean = (float)((double)sumq / 1099511627776.0 / (double)L);
     if (bad_flags) {
         if (tid == 0) {
-            a.status[b] = EB_STATUS_NONFINITE | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
+            a.status[b] = ((bad_flags & 1) ? EB_STATUS_NONFINITE : 0) | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
             if (a.steps_taken) a.steps_taken[b] = a.step + 1;
             if (a.committed) a.committed[b] = 0;
             if (a.mean_entropy) a.mean_entropy[b] = NAN;

@@ -20,7 +20,8 @@ EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
 
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
-            "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events")
+            "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",
+            "eb_unembed_workspace_bytes", "eb_unembed_sample", "eb_unembed_logits")
 
 
 class EbParams(ctypes.Structure):
@@ -72,6 +73,13 @@ def lib() -> ctypes.CDLL:
     L.eb_last_error.restype = ctypes.c_char_p
     L.eb_set_profile_events.argtypes = [P, P]
     L.eb_set_profile_events.restype = i32
+    L.eb_unembed_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.eb_unembed_workspace_bytes.restype = sz
+    L.eb_unembed_sample.argtypes = ([ctypes.POINTER(EbParams), i32, i32, i32, i32, P, P, i32,
+                                     ctypes.c_float] + [P] * 11 + [P, sz, P])
+    L.eb_unembed_sample.restype = i32
+    L.eb_unembed_logits.argtypes = [i32, i32, i32, P, P, P, P]
+    L.eb_unembed_logits.restype = i32
     _lib = L
     return L
 
@@ -146,6 +154,26 @@ def eb_sample_canvas(params: EbParams, B: int, L: int, V: int, dtype: int, logit
     return ran.value
 
 
+def eb_unembed_workspace_bytes(B: int, L: int, K: int, V: int) -> int:
+    return int(lib().eb_unembed_workspace_bytes(B, L, K, V))
+
+
+def eb_unembed_sample(params: EbParams, B: int, L: int, K: int, V: int, h, W, step: int,
+                      temperature: float, mask, tokens, prev_argmax, status, steps_taken,
+                      entropy, argmax, sampled, selected, committed, mean_entropy,
+                      workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib().eb_unembed_sample(ctypes.byref(params), B, L, K, V, _ptr(h), _ptr(W), step,
+                                   float(temperature), _ptr(mask), _ptr(tokens),
+                                   _ptr(prev_argmax), _ptr(status), _ptr(steps_taken),
+                                   _ptr(entropy), _ptr(argmax), _ptr(sampled), _ptr(selected),
+                                   _ptr(committed), _ptr(mean_entropy), _ptr(workspace),
+                                   workspace_bytes, _stream(stream)))
+
+
+def eb_unembed_logits(M: int, K: int, V: int, h, W, logits, stream=None) -> None:
+    _check(lib().eb_unembed_logits(M, K, V, _ptr(h), _ptr(W), _ptr(logits), _stream(stream)))
+
+
 def eb_set_profile_events(k1_begin, k1_end) -> None:
     """torch.cuda.Event pair (or raw cudaEvent_t ints) around the next row-statistics launch."""
     def ev(e):
@@ -189,6 +217,21 @@ class Canvas:
                         self.mask, self.tokens, self.prev_argmax, self.status, self.steps_taken,
                         self.entropy, self.argmax, self.sampled, self.selected, self.committed,
                         self.mean_entropy, self.workspace, self.ws_bytes, stream)
+
+    def unembed_step(self, params: EbParams, h, W, K: int, step: int, temperature: float = 0.0,
+                     workspace=None, stream=None):
+        """One fused unembedding + sampler step: logits = h W never leave the chip.  Uses a
+        workspace of eb_unembed_workspace_bytes (allocated on first use unless given)."""
+        import torch
+        need = eb_unembed_workspace_bytes(self.B, self.L, K, self.V)
+        if workspace is None:
+            if getattr(self, "_uws", None) is None or self._uws.numel() < need:
+                self._uws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.mask.device)
+            workspace = self._uws
+        eb_unembed_sample(params, self.B, self.L, K, self.V, h, W, step, temperature, self.mask,
+                          self.tokens, self.prev_argmax, self.status, self.steps_taken,
+                          self.entropy, self.argmax, self.sampled, self.selected,
+                          self.committed, self.mean_entropy, workspace, need, stream)
 
     def run(self, params: EbParams, logits_fn, user, logits, start_step: int = 0,
             poll_every: int = 0, stream=None) -> int:

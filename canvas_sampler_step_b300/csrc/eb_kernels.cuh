@@ -132,6 +132,9 @@ struct K2Args {
     float c;
     long long bound_q;         // entropy_bound in 2^-40 nats (rounded down)
     long long stop_q;          // stop_entropy * L in 2^-40 nats (rounded up): mean < stop
+    int k3_g;                  // > 0: partials come from the fused unembedding kernel, whose
+                               // row block mb, group rank j < k3_g and column half hh write
+                               // slot ((mb k3_g + j) 2 + hh) 128 + row % 128
 };
 
 // ---------------------------------------------------------------- small device helpers

@@ -451,7 +451,17 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const unsigned long long w0 = k2_row_start(a, r), w1 = k2_row_start(a, r + 1);
         RowState st = empty_state();
         int flags = 0;
-        if (w1 > w0) {
+        if (a.k3_g > 0) {
+            const long long mb = r >> 7, rl = r & 127;
+            for (int j = 0; j < a.k3_g; ++j) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const Partial q = a.partials[((mb * a.k3_g + j) * 2 + hh) * 128 + rl];
+                    merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
+                    flags |= q.flags;
+                }
+            }
+        } else if (w1 > w0) {
             const int c0 = (int)(((w0 + 1) * G - 1) / W);
             const int c1 = (int)((w1 * G - 1) / W);
             for (int c = c0; c <= c1; ++c) {
@@ -663,6 +673,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
 
 }  // namespace ebk
 
+// the fused unembedding kernel reuses the partial-state helpers above
+#include "eb_unembed.cuh"
+
 // ====================================================================== host side
 
 namespace {
@@ -738,6 +751,83 @@ eb_status geometry(int *grid_out, int kind)
     return EB_OK;
 }
 
+// Per-device set-up of the fused unembedding kernel: SM count and its shared-memory limit.
+struct UnembedGeometry {
+    std::atomic<int> ready{0};
+    int nsm = 0;
+};
+UnembedGeometry g_unembed[64];
+
+eb_status unembed_geometry(int *nsm_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(EB_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= 64) return fail(EB_ERR_UNSUPPORTED, "device index %d >= 64", dev);
+    UnembedGeometry &g = g_unembed[dev];
+    if (g.ready.load(std::memory_order_acquire) == 0) {
+        int nsm = 0, smem_optin = 0, major = 0;
+        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            return fail(EB_ERR_CUDA, "cudaDeviceGetAttribute failed");
+        if (major != 10) return fail(EB_ERR_UNSUPPORTED, "the fused unembedding kernel needs tcgen05 (sm_10x)");
+        const size_t smem = ebk::k3::Smem::alloc;
+        if ((size_t)smem_optin < smem)
+            return fail(EB_ERR_UNSUPPORTED, "device offers %d B of shared memory per block, need %zu",
+                        smem_optin, smem);
+        if (cudaFuncSetAttribute(ebk::k3::k3_unembed<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(ebk::k3::k3_unembed<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
+        g.nsm = nsm;
+        g.ready.store(1, std::memory_order_release);
+    }
+    *nsm_out = g.nsm;
+    return EB_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver (looked up once through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// 2-D bf16 tensor map of a row-major [outer, inner] matrix (inner contiguous) with a
+// box_inner x box_outer box and 128-byte swizzle; out-of-range elements read as zero.
+eb_status encode_bf16_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                         uint32_t box_outer)
+{
+    EncodeTiledFn f = encode_fn();
+    if (!f) return fail(EB_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(EB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return EB_OK;
+}
+
 ebk::RoundKeys round_keys(uint64_t seed)
 {
     ebk::RoundKeys K;
@@ -774,7 +864,8 @@ struct StepBuffers {
 };
 
 eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dtype,
-                       const void *d_logits, const StepBuffers &sb, void *d_ws, size_t ws_bytes)
+                       const void *d_logits, const StepBuffers &sb, void *d_ws, size_t ws_bytes,
+                       size_t ws_needed)
 {
     if (!params) return fail(EB_ERR_INVALID, "params is NULL");
     if (params->flags != 0) return fail(EB_ERR_INVALID, "params->flags must be 0");
@@ -798,9 +889,47 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
     if (rows > (1ll << 31) - 1 - ebk::kMaxGrid) return fail(EB_ERR_UNSUPPORTED, "B*L too large");
     if (!d_ws) return fail(EB_ERR_WORKSPACE, "workspace is NULL");
     if (((uintptr_t)d_ws & 255) != 0) return fail(EB_ERR_WORKSPACE, "workspace not 256-byte aligned");
-    if (ws_bytes < eb_workspace_bytes(B, L, V, dtype))
-        return fail(EB_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes,
-                    eb_workspace_bytes(B, L, V, dtype));
+    if (ws_bytes < ws_needed)
+        return fail(EB_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, ws_needed);
+    return EB_OK;
+}
+
+// Enqueues the selection kernel over the partial states of this step.
+eb_status launch_select(const eb_params *params, int B, int L, int step, float c, const StepBuffers &sb,
+                        const ebk::Partial *partials, const uint32_t *prefix, long long nvec_row,
+                        int rows, int G, int weighted, int k3_g, cudaStream_t stream)
+{
+    ebk::K2Args a2;
+    a2.partials = partials;
+    a2.prefix = prefix;
+    a2.mask = sb.mask;
+    a2.tokens = sb.tokens;
+    a2.prev_argmax = sb.prev_argmax;
+    a2.status = sb.status;
+    a2.steps_taken = sb.steps_taken;
+    a2.entropy = sb.entropy;
+    a2.argmax = sb.argmax;
+    a2.sampled = sb.sampled;
+    a2.selected = sb.selected;
+    a2.committed = sb.committed;
+    a2.mean_entropy = sb.mean_entropy;
+    a2.committed_hist = sb.committed_hist;
+    a2.mean_hist = sb.mean_hist;
+    a2.nvec_row = nvec_row;
+    a2.rows = rows;
+    a2.L = L;
+    a2.G = G;
+    a2.step = step;
+    a2.max_steps = params->max_steps;
+    a2.weighted = weighted;
+    a2.c = c;
+    // fixed point, 2^-40 nats: accept while prefix <= floor(bound), stop while sum < ceil(stop L)
+    a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
+    a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
+    a2.k3_g = k3_g;
+    ebk::k2_select<<<B, ebk::kK2Threads, 0, stream>>>(a2);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "selection launch: %s", cudaGetErrorString(e));
     return EB_OK;
 }
 
@@ -861,37 +990,72 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     if (prof_end && cudaEventRecord(prof_end, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
 
-    ebk::K2Args a2;
-    a2.partials = partials;
-    a2.prefix = prefix;
-    a2.mask = sb.mask;
-    a2.tokens = sb.tokens;
-    a2.prev_argmax = sb.prev_argmax;
-    a2.status = sb.status;
-    a2.steps_taken = sb.steps_taken;
-    a2.entropy = sb.entropy;
-    a2.argmax = sb.argmax;
-    a2.sampled = sb.sampled;
-    a2.selected = sb.selected;
-    a2.committed = sb.committed;
-    a2.mean_entropy = sb.mean_entropy;
-    a2.committed_hist = sb.committed_hist;
-    a2.mean_hist = sb.mean_hist;
-    a2.nvec_row = nvec_row;
-    a2.rows = (int)rows;
-    a2.L = L;
-    a2.G = G;
-    a2.step = step;
-    a2.max_steps = params->max_steps;
-    a2.weighted = a1.weighted;
-    a2.c = a1.c;
-    // fixed point, 2^-40 nats: accept while prefix <= floor(bound), stop while sum < ceil(stop L)
-    a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
-    a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
-    ebk::k2_select<<<B, ebk::kK2Threads, 0, stream>>>(a2);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "selection launch: %s", cudaGetErrorString(e));
-    return EB_OK;
+    return launch_select(params, B, L, step, a1.c, sb, partials, prefix, nvec_row, (int)rows, G,
+                         a1.weighted, 0, stream);
+}
+
+// Enqueues the fused unembedding kernel (+ the selection kernel unless logits_out is given).
+// Arguments were validated by the caller.
+eb_status launch_unembed(const eb_params *params, int B, int L, int K, int V, const void *d_h,
+                         const void *d_W, int step, float T, const StepBuffers *sb, void *d_ws,
+                         float *logits_out, cudaStream_t stream)
+{
+    namespace k3 = ebk::k3;
+    int nsm = 0;
+    eb_status st = unembed_geometry(&nsm);
+    if (st != EB_OK) return st;
+    const long long M = (long long)B * L;
+    const int MB = (int)((M + k3::BM - 1) / k3::BM);
+    const int NB = (int)(((long long)V + k3::BN - 1) / k3::BN);
+    const int KB = (K + k3::BK - 1) / k3::BK;
+    const int Gmax = nsm < k3::kMaxCtas ? nsm : k3::kMaxCtas;
+    int g, G;
+    if (MB <= Gmax) {
+        g = Gmax / MB;
+        if (g > NB) g = NB;
+        G = MB * g;
+    } else {
+        g = 1;
+        G = Gmax;
+    }
+    CUtensorMap th, tw;
+    st = encode_bf16_2d(&th, d_h, (uint64_t)K, (uint64_t)M, k3::BK, k3::BM);
+    if (st != EB_OK) return st;
+    st = encode_bf16_2d(&tw, d_W, (uint64_t)V, (uint64_t)K, 64, k3::BK);
+    if (st != EB_OK) return st;
+
+    k3::Args a;
+    a.mask = sb ? sb->mask : nullptr;
+    a.status = sb ? sb->status : nullptr;
+    a.partials = static_cast<ebk::Partial *>(d_ws);
+    a.logits = logits_out;
+    a.M = (int)M;
+    a.K = K;
+    a.V = V;
+    a.L = L;
+    a.MB = MB;
+    a.NB = NB;
+    a.KB = KB;
+    a.g = g;
+    a.G = G;
+    a.step = step;
+    a.c = ebk::kLog2e / T;
+    a.invT = 1.0f / T;
+    a.keys = round_keys(params ? params->seed : 0);
+    cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
+    g_profile_begin = g_profile_end = nullptr;
+    if (prof_begin && cudaEventRecord(prof_begin, stream) != cudaSuccess)
+        return fail(EB_ERR_CUDA, "cudaEventRecord failed");
+    if (logits_out)
+        k3::k3_unembed<true><<<G, k3::kThreads, k3::Smem::alloc, stream>>>(th, tw, a);
+    else
+        k3::k3_unembed<false><<<G, k3::kThreads, k3::Smem::alloc, stream>>>(th, tw, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "unembedding launch: %s", cudaGetErrorString(e));
+    if (prof_end && cudaEventRecord(prof_end, stream) != cudaSuccess)
+        return fail(EB_ERR_CUDA, "cudaEventRecord failed");
+    if (logits_out) return EB_OK;
+    return launch_select(params, B, L, step, a.c, *sb, a.partials, nullptr, 0, (int)M, G, 0, g, stream);
 }
 
 }  // namespace
@@ -935,7 +1099,8 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
 {
     StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
                    d_sampled, d_selected, d_committed, d_mean_entropy, nullptr, nullptr};
-    eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, d_workspace, workspace_bytes);
+    eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, d_workspace, workspace_bytes,
+                                eb_workspace_bytes(B, L, V, dtype));
     if (st != EB_OK) return st;
     if (B == 0) return ok();
     if (step < 0 || step >= params->max_steps)
@@ -961,7 +1126,8 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
     StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
                    d_sampled, d_selected, nullptr, nullptr, d_committed_per_step,
                    d_mean_entropy_per_step};
-    eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, d_workspace, workspace_bytes);
+    eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, d_workspace, workspace_bytes,
+                                eb_workspace_bytes(B, L, V, dtype));
     if (st != EB_OK) return st;
     if (!logits_fn) return fail(EB_ERR_INVALID, "logits_fn is NULL");
     if (start_step < 0) return fail(EB_ERR_INVALID, "start_step must be >= 0");
@@ -1001,6 +1167,73 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
     }
     if (steps_run) *steps_run = ran;
     return ok();
+}
+
+size_t eb_unembed_workspace_bytes(int B, int L, int K, int V)
+{
+    (void)K;
+    (void)V;
+    if (B < 0 || L < 1) return 0;
+    const long long M = (long long)B * L;
+    const long long MB = (M + ebk::k3::BM - 1) / ebk::k3::BM;
+    const long long slots = MB > ebk::k3::kMaxCtas ? MB : ebk::k3::kMaxCtas;
+    return align256((size_t)slots * 2 * ebk::k3::BM * sizeof(ebk::Partial));
+}
+
+namespace {
+
+eb_status check_unembed(int M, int K, int V, const void *d_h, const void *d_W)
+{
+    if (M < 0) return fail(EB_ERR_INVALID, "B*L must be >= 0");
+    if (K < 8 || K % 8 != 0) return fail(EB_ERR_INVALID, "K must be a positive multiple of 8 (got %d)", K);
+    if (V < 8 || V % 8 != 0) return fail(EB_ERR_INVALID, "V must be a positive multiple of 8 (got %d)", V);
+    if (M == 0) return EB_OK;
+    if (!d_h || !d_W) return fail(EB_ERR_INVALID, "d_h / d_W is NULL");
+    if (((uintptr_t)d_h & 15) || ((uintptr_t)d_W & 15))
+        return fail(EB_ERR_INVALID, "d_h and d_W must be 16-byte aligned");
+    return EB_OK;
+}
+
+}  // namespace
+
+eb_status eb_unembed_sample(const eb_params *params, int B, int L, int K, int V, const void *d_h,
+                            const void *d_W, int step, float temperature, uint8_t *d_mask,
+                            int32_t *d_tokens, int32_t *d_prev_argmax, int32_t *d_status,
+                            int32_t *d_steps_taken, float *d_entropy, int32_t *d_argmax,
+                            int32_t *d_sampled, uint8_t *d_selected, int32_t *d_committed,
+                            float *d_mean_entropy, void *d_workspace, size_t workspace_bytes,
+                            void *stream)
+{
+    StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
+                   d_sampled, d_selected, d_committed, d_mean_entropy, nullptr, nullptr};
+    eb_status st = check_common(params, B, L, V, EB_BF16, d_h, sb, d_workspace, workspace_bytes,
+                                eb_unembed_workspace_bytes(B, L, K, V));
+    if (st != EB_OK) return st;
+    if (B == 0) return ok();
+    st = check_unembed(B * L, K, V, d_h, d_W);
+    if (st != EB_OK) return st;
+    if (step < 0 || step >= params->max_steps)
+        return fail(EB_ERR_INVALID, "step %d outside [0, max_steps=%d)", step, params->max_steps);
+    if (std::isnan(temperature) || std::isinf(temperature))
+        return fail(EB_ERR_INVALID, "temperature must be finite");
+    const float T = temperature > 0.0f ? temperature : schedule_temperature(params, step);
+    st = launch_unembed(params, B, L, K, V, d_h, d_W, step, T, &sb, d_workspace, nullptr,
+                        static_cast<cudaStream_t>(stream));
+    return st == EB_OK ? ok() : st;
+}
+
+eb_status eb_unembed_logits(int M, int K, int V, const void *d_h, const void *d_W, float *d_logits,
+                            void *stream)
+{
+    eb_status st = check_unembed(M, K, V, d_h, d_W);
+    if (st != EB_OK) return st;
+    if (M == 0) return ok();
+    if (!d_logits) return fail(EB_ERR_INVALID, "d_logits is NULL");
+    if (M > (1 << 30)) return fail(EB_ERR_UNSUPPORTED, "M too large");
+    // one canvas of M positions as far as the launch geometry is concerned
+    st = launch_unembed(nullptr, 1, M, K, V, d_h, d_W, 0, 1.0f, nullptr, nullptr, d_logits,
+                        static_cast<cudaStream_t>(stream));
+    return st == EB_OK ? ok() : st;
 }
 
 const char *eb_status_string(eb_status s)

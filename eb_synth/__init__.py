@@ -42,6 +42,9 @@ import numpy as np
 STREAM_NORMAL = 2
 STREAM_POSITION = 3
 STREAM_MASK = 4
+STREAM_UNEMBED_H = 5
+STREAM_UNEMBED_COL = 6
+STREAM_UNEMBED_W = 7
 
 _F = np.float32
 _M0 = np.uint64(0xD2511F53)
@@ -165,11 +168,17 @@ def _sincos_2pi(u: np.ndarray):
 
 def normals(seed: int, b: int, p, s: int, V: int) -> np.ndarray:
     """Background normals n[b, p, v] for the given positions p (array), shape [len(p), V]."""
-    p = np.atleast_1d(np.asarray(p, np.int64))
+    return _normal_rows(seed, p, s, (STREAM_NORMAL << 24) | b, V)
+
+
+def _normal_rows(seed: int, rows, c2: int, c3: int, cols: int) -> np.ndarray:
+    """Box-Muller normals of counters (k, row, c2, c3), k = column // 4: [len(rows), cols]."""
+    p = np.atleast_1d(np.asarray(rows, np.int64))
+    V = cols
     nk = (V + 3) // 4
     k = np.arange(nk, dtype=np.uint64)[None, :]
     pc = p.astype(np.uint64)[:, None]
-    w0, w1, w2, w3 = philox(k, pc, np.uint64(s), np.uint64((STREAM_NORMAL << 24) | b), seed)
+    w0, w1, w2, w3 = philox(k, pc, np.uint64(c2), np.uint64(c3), seed)
     r0 = np.sqrt(_ln(uniform(w0)) * _F(-2.0))
     r1 = np.sqrt(_ln(uniform(w2)) * _F(-2.0))
     c0, s0 = _sincos_2pi(uniform(w1))
@@ -275,3 +284,61 @@ CFG3_RATES = (0.1, 0.2, 0.4, 0.8)
 def cfg3(B: int = 8, L: int = 256, V: int = 262144) -> Peaked:
     return Peaked(B, L, V, "bf16", 3.0, 0.0, 4.0,
                   tuple(CFG3_RATES[b % 4] for b in range(B)), tuple(range(B)))
+
+
+# ------------------------------------------------------------------ fused unembedding inputs
+
+def unembed_h_rows(seed: int, rows, K: int) -> np.ndarray:
+    """Hidden states h[m, :] = N(0,1) for rows m (array) as bf16 bits [len(rows), K];
+    counters (j // 4, m, 0, 5 << 24)."""
+    n = _normal_rows(seed, rows, 0, STREAM_UNEMBED_H << 24, K)
+    return to_bf16_bits((n * _F(1.0)).astype(_F))
+
+
+def unembed_bias_columns(seed: int, rows, V: int) -> np.ndarray:
+    """Column c_k = (w0 * V) >> 32 of counter (0, k, 0, 6 << 24) that carries row k's bias."""
+    rows = np.atleast_1d(np.asarray(rows, np.uint64))
+    w0, _, _, _ = philox(np.uint64(0), rows, np.uint64(0), np.uint64(STREAM_UNEMBED_COL << 24), seed)
+    return ((w0.astype(np.uint64) * np.uint64(V)) >> np.uint64(32)).astype(np.int64)
+
+
+def unembed_W_rows(seed: int, rows, V: int, sigma_w: float = 0.02, bias: float = 0.05) -> np.ndarray:
+    """Unembedding rows W[k, :] = sigma_w N(0,1) plus `bias` at column c_k, for rows k (array),
+    as bf16 bits [len(rows), V]; counters (v // 4, k, 0, 7 << 24)."""
+    rows = np.atleast_1d(np.asarray(rows, np.int64))
+    x = (_normal_rows(seed, rows, 0, STREAM_UNEMBED_W << 24, V) * _F(sigma_w)).astype(_F)
+    c = unembed_bias_columns(seed, rows, V)
+    idx = np.arange(rows.shape[0])
+    x[idx, c] = (x[idx, c] + _F(bias)).astype(_F)
+    return to_bf16_bits(x)
+
+
+@dataclass(frozen=True)
+class Unembed:
+    """Recipe of the fused unembedding workload: h [B*L, K] ~ N(0,1), W [K, V] ~
+    N(0, sigma_w^2) with +bias planted at one seeded column per row of W, both bf16."""
+    B: int
+    L: int
+    K: int
+    V: int
+    seed: int = 0
+    sigma_w: float = 0.02
+    bias: float = 0.05
+
+    @property
+    def M(self) -> int:
+        return self.B * self.L
+
+    def h(self) -> np.ndarray:
+        return unembed_h_rows(self.seed, np.arange(self.M), self.K)
+
+    def W(self, rows_per_chunk: int = 64) -> np.ndarray:
+        out = np.empty((self.K, self.V), np.uint16)
+        for k0 in range(0, self.K, rows_per_chunk):
+            k = np.arange(k0, min(self.K, k0 + rows_per_chunk))
+            out[k0:k0 + k.shape[0]] = unembed_W_rows(self.seed, k, self.V, self.sigma_w, self.bias)
+        return out
+
+
+def cfg4(B: int = 4, L: int = 256, K: int = 2048, V: int = 262144, seed: int = 0) -> Unembed:
+    return Unembed(B, L, K, V, seed)

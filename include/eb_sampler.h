@@ -154,10 +154,44 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
                            uint8_t *d_selected, void *d_workspace, size_t workspace_bytes,
                            int poll_every, int *steps_run, void *stream);
 
+/*
+ * Fused unembedding + sampler step.  The logits of the step are the product of the decoder's
+ * final hidden states and the unembedding matrix, logits = h W (the model card's decoder
+ * emits full-vocabulary logits for every canvas position at every step, "Best practices"
+ * section 1 consumes them); this entry point computes that product on the tensor cores and
+ * feeds every accumulator tile straight into the row statistics of item 2, so the [B*L, V]
+ * logits are never written to memory.  Items 1-5 then run exactly as in eb_sampler_step, on
+ * the fp32 accumulator values as the raw logits.
+ *
+ *   B, L           canvases and positions per canvas; M = B * L rows of h
+ *   K              hidden width (a positive multiple of 8)
+ *   V              vocabulary (a positive multiple of 8)
+ *   d_h            [M, K] bf16, row-major (K contiguous), 16-byte aligned (read only)
+ *   d_W            [K, V] bf16, row-major (V contiguous), 16-byte aligned (read only)
+ *   the other arguments as in eb_sampler_step; the workspace must hold
+ *   eb_unembed_workspace_bytes(B, L, K, V) bytes, 256-byte aligned.
+ * Needs a device with tcgen05 tensor cores (sm_10x); EB_ERR_UNSUPPORTED otherwise.
+ */
+size_t eb_unembed_workspace_bytes(int B, int L, int K, int V);
+
+eb_status eb_unembed_sample(const eb_params *params, int B, int L, int K, int V, const void *d_h,
+                            const void *d_W, int step, float temperature, uint8_t *d_mask,
+                            int32_t *d_tokens, int32_t *d_prev_argmax, int32_t *d_status,
+                            int32_t *d_steps_taken, float *d_entropy, int32_t *d_argmax,
+                            int32_t *d_sampled, uint8_t *d_selected, int32_t *d_committed,
+                            float *d_mean_entropy, void *d_workspace, size_t workspace_bytes,
+                            void *stream);
+
+/* The same tensor-core product written out: d_logits [M, V] fp32 (row-major) = h W with h
+ * [M, K] and W [K, V] bf16 as above.  For callers that need the logits themselves. */
+eb_status eb_unembed_logits(int M, int K, int V, const void *d_h, const void *d_W, float *d_logits,
+                            void *stream);
+
 /* Instrumentation: CUDA events (cudaEvent_t as void*) to record on the stream right
- * before and right after the row-statistics kernel of the NEXT eb_sampler_step /
- * eb_sample_canvas step enqueued by the calling thread (one-shot; NULL, NULL clears).
- * Lets a caller time the bandwidth-bound kernel alone with CUDA events. */
+ * before and right after the row-statistics kernel (the streaming one, or the fused
+ * unembedding one) of the NEXT eb_sampler_step / eb_sample_canvas step / eb_unembed_sample /
+ * eb_unembed_logits call enqueued by the calling thread (one-shot; NULL, NULL clears).
+ * Lets a caller time the dominant kernel alone with CUDA events. */
 eb_status eb_set_profile_events(void *k1_begin, void *k1_end);
 
 /* Short English name of a status code (static storage). */

@@ -15,6 +15,8 @@ row(x, T, masked, ...)     -- entropy, argmax and Gumbel-max sample of one row
 select(H, mask, bound)     -- entropy-bounded prefix selection of one canvas
 step(...)                  -- one full sampler step over B canvases (stats, stop test,
                               selection, re-mask, complete / cap)
+unembed_logits(h, W)       -- the decoder's unembedding product h W in binary64 (the logits
+                              the fused path feeds to the sampler without storing them)
 run_loop(...)              -- the <= 48-step denoising loop with per-canvas stop
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py`` except the
@@ -251,3 +253,17 @@ def run_loop(logits_fn, B: int, L: int, params: Params = Params(), state: State 
         if on_step is not None:
             on_step(s, res, st)
     return st
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact binary64 values of bfloat16 bit patterns (uint16)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def unembed_logits(h_bits: np.ndarray, W_bits: np.ndarray) -> np.ndarray:
+    """logits = h W in binary64 for bf16 h [M, K] and W [K, V] (bit patterns).  The sampler
+    step consumes the decoder's full-vocabulary logits of every canvas position (DiffusionGemma
+    model card, "Best practices" section 1); the fused path computes them as this product.
+    numpy's matmul serves as the (library) dot-product step; every product of two bfloat16
+    values is exact in binary64, so the only rounding is binary64 accumulation."""
+    return bf16_to_f64(h_bits) @ bf16_to_f64(W_bits)

@@ -53,9 +53,13 @@ class Report:
 
 
 def compare_step(g: dict, res: oracle.StepResult, ost: oracle.State, running_before: np.ndarray,
-                 rep: Report, ctx: str = "") -> set:
+                 rep: Report, ctx: str = "", atie: np.ndarray | None = None,
+                 ytie_extra: np.ndarray | None = None) -> set:
     """Compare one GPU step (host copies ``g``) with the oracle's result ``res`` / state
-    ``ost``.  Returns the set of canvases that hit a tie at this step."""
+    ``ost``.  Returns the set of canvases that hit a tie at this step.  ``atie`` / ``ytie_extra``
+    ([B, L] bool, optional) mark rows where the GPU's logits themselves carry a rounding
+    error (the fused product) large enough to swap the argmax / the sample: those rows are
+    counted as ties too, and a canvas holding one is not compared beyond its rows."""
     B, L = res.H.shape
     tied = set()
     for b in range(B):
@@ -66,13 +70,21 @@ def compare_step(g: dict, res: oracle.StepResult, ost: oracle.State, running_bef
         herr = np.abs(g["entropy"][b].astype(np.float64) - res.H[b])
         rep.max_h_err = max(rep.max_h_err, float(herr.max()))
         assert herr.max() <= H_TOL, f"{ctx} canvas {b}: entropy error {herr.max():.3g}"
-        assert np.array_equal(g["argmax"][b], res.A[b]), f"{ctx} canvas {b}: argmax differs"
+        a_ok = g["argmax"][b] == res.A[b]
+        if atie is not None:
+            rep.row_ties += int((atie[b] & ~a_ok).sum())
+            a_ok |= atie[b]
+        assert a_ok.all(), f"{ctx} canvas {b}: argmax differs at {np.nonzero(~a_ok)[0][:8]}"
         ytie = res.gap[b] < GAP_TOL
+        if ytie_extra is not None:
+            ytie = ytie | ytie_extra[b]
         rep.row_ties += int(ytie.sum())
         ok_y = (g["sampled"][b] == res.Y[b]) | ytie
         assert ok_y.all(), f"{ctx} canvas {b}: sampled token differs at {np.nonzero(~ok_y)[0][:8]}"
         ctie = (res.sum_margin[b] < SUM_TOL or res.order_margin[b] < ORDER_TOL
                 or res.stop_margin[b] < STOP_TOL)
+        if atie is not None and (atie[b] & (g["argmax"][b] != res.A[b])).any():
+            ctie = True     # a swapped argmax feeds the stop test and the finalisation
         if ctie:
             rep.canvas_ties += 1
             tied.add(b)

@@ -1,0 +1,185 @@
+"""GPU-vs-oracle parity of the fused unembedding + sampler step (tcgen05 tensor-core product
+whose epilogue runs the sampler's row statistics; the logits never reach memory).
+
+The oracle forms the logits h W in binary64 from the same bf16 inputs (numpy generator) and
+runs its sampler step on them.  The GPU accumulates in fp32 on the tensor cores, so each of
+its logits may differ from the binary64 value by up to K 2^-23 sum_k |h_k W_kv|; rows whose
+top-2 raw logits (argmax) or top-2 perturbed scores (sample) lie within twice that bound are
+counted as ties, in addition to the streaming path's tie rules.
+"""
+import numpy as np
+import pytest
+import torch
+
+import canvas_sampler_step_b300 as eb
+import eb_synth
+import eb_synth.device as synth_dev
+import oracle
+from parity import Report, compare_step, host_state, params_pair, H_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    eb.build()
+    synth_dev.build()
+    eb.lib()
+    synth_dev.lib()
+
+
+def _dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def _error_bound(h_bits, W_bits):
+    """Per-element bound K 2^-23 (|h| |W|) on an fp32 accumulation of the K products."""
+    K = h_bits.shape[1]
+    return K * 2.0 ** -23 * (np.abs(oracle.bf16_to_f64(h_bits)) @ np.abs(oracle.bf16_to_f64(W_bits)))
+
+
+def _ties(x64: np.ndarray, bound: np.ndarray, gap: np.ndarray, T: float):
+    """(argmax tie, sample tie) masks of rows [M] from the binary64 logits and the bound."""
+    E = bound.max(axis=1)
+    top2 = -np.partition(-x64, 1, axis=1)[:, :2]
+    atie = (top2[:, 0] - top2[:, 1]) < 2.0 * E
+    ytie = gap < 2.0 * E / T
+    return atie, ytie
+
+
+@pytest.mark.parametrize("M,K,V", [(128, 64, 256), (300, 200, 1000), (1024, 2048, 4096)])
+def test_unembed_logits_match_binary64(M, K, V):
+    u = eb_synth.Unembed(1, M, K, V, seed=3)
+    hb, Wb = u.h(), u.W()
+    out = torch.full((M, V), float("nan"), dtype=torch.float32, device="cuda")
+    eb.eb_unembed_logits(M, K, V, _dev(hb), _dev(Wb), out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    ref = oracle.unembed_logits(hb, Wb)
+    bound = _error_bound(hb, Wb)
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert (err <= bound + 1e-30).all(), f"max err {err.max():.3g} vs bound {bound.max():.3g}"
+
+
+def _fused_vs_oracle(B, L, K, V, mask, seed=0, temperature=0.8):
+    u = eb_synth.Unembed(B, L, K, V, seed=seed)
+    hb, Wb = u.h(), u.W()
+    gp, op = params_pair(seed=seed)
+    c = eb.Canvas(B, L, V, eb.EB_BF16, mask=mask)
+    c.unembed_step(gp, _dev(hb), _dev(Wb), K, 0, temperature)
+    g = host_state(c)
+    x64 = oracle.unembed_logits(hb, Wb)
+    ost = oracle.State.fresh(B, L, mask)
+    T = float(np.float32(temperature))
+    res = oracle.step(x64.reshape(B, L, V), ost, 0, op, temperature=T)
+    atie, ytie = _ties(x64, _error_bound(hb, Wb), res.gap.reshape(-1), T)
+    rep = Report()
+    compare_step(g, res, ost, np.ones(B, bool), rep, ctx=f"fused {B}x{L}x{K}x{V}",
+                 atie=atie.reshape(B, L), ytie_extra=ytie.reshape(B, L))
+    return rep, g, res
+
+
+@pytest.mark.parametrize("B,L,K,V,density", [
+    (2, 64, 256, 4096, 1.0),        # one row block, 16 column tiles
+    (3, 100, 512, 20000, 0.5),      # ragged row block (M = 300) and column tail (V % 256 != 0)
+    (1, 256, 2048, 8192, 1.0),      # the workload's hidden width
+])
+def test_unembed_sample_parity(B, L, K, V, density):
+    rng = np.random.default_rng(B * 1000 + V)
+    mask = (rng.random((B, L)) < density).astype(np.uint8)
+    mask[:, 0] = 1
+    rep, g, res = _fused_vs_oracle(B, L, K, V, mask)
+    assert rep.max_h_err < H_TOL
+    assert rep.canvas_ties <= max(1, B // 2)
+
+
+def test_unembed_equals_written_logits_through_streaming_path():
+    """The fused step and (written-out logits -> streaming step) agree: same accumulators,
+    same per-entry arithmetic, only the summation order of the entropy differs."""
+    B, L, K, V = 2, 128, 512, 16384
+    u = eb_synth.Unembed(B, L, K, V, seed=7)
+    h, W = _dev(u.h()), _dev(u.W())
+    gp, _ = params_pair(seed=7)
+    fused = eb.Canvas(B, L, V, eb.EB_BF16)
+    fused.unembed_step(gp, h, W, K, 0, 0.8)
+    logits = torch.empty((B, L, V), dtype=torch.float32, device="cuda")
+    eb.eb_unembed_logits(B * L, K, V, h, W, logits)
+    streamed = eb.Canvas(B, L, V, eb.EB_F32)
+    streamed.step(gp, logits, 0, 0.8)
+    a, b = host_state(fused), host_state(streamed)
+    assert np.abs(a["entropy"] - b["entropy"]).max() < 2e-5
+    assert np.array_equal(a["argmax"], b["argmax"])
+    assert np.array_equal(a["sampled"], b["sampled"])
+    assert np.array_equal(a["selected"], b["selected"])
+    assert np.array_equal(a["tokens"], b["tokens"])
+
+
+def test_unembed_full_size_sampled_rows():
+    """B=4 canvases x 256 positions, K=2048, V=262144, all masked, T=0.8 (the fused workload
+    as the benchmark launches it): device inputs equal the numpy generator's, and sampled
+    rows match the oracle one by one."""
+    B, L, K, V = 4, 256, 2048, 262144
+    u = eb_synth.cfg4()
+    h = torch.empty((B * L, K), dtype=torch.int16, device="cuda")
+    W = torch.empty((K, V), dtype=torch.int16, device="cuda")
+    synth_dev.unembed_inputs(u.seed, B * L, K, V, u.sigma_w, u.bias, h, W)
+    hb = u.h()
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), hb)
+    gp, op = params_pair(seed=0)
+    c = eb.Canvas(B, L, V, eb.EB_BF16)
+    c.unembed_step(gp, h, W, K, 0, 0.8)
+    g = host_state(c)
+    assert (g["status"] == eb.EB_RUNNING).all() and (g["committed"] >= 1).all()
+    rows = np.array([0, 1, 127, 128, 300, 511, 640, 1023])
+    # binary64 logits of the sampled rows, accumulated over the numpy W in row chunks;
+    # the device W is compared with the numpy W chunk by chunk on the way
+    Wd = W.cpu().numpy().view(np.uint16)
+    x64 = np.zeros((rows.shape[0], V))
+    absx = np.zeros((rows.shape[0], V))
+    hf = oracle.bf16_to_f64(hb[rows])
+    for k0 in range(0, K, 64):
+        kk = np.arange(k0, k0 + 64)
+        Wn = eb_synth.unembed_W_rows(u.seed, kk, V, u.sigma_w, u.bias)
+        assert np.array_equal(Wn, Wd[k0:k0 + 64]), f"generator rows {k0}.."
+        Wf = oracle.bf16_to_f64(Wn)
+        x64 += hf[:, k0:k0 + 64] @ Wf
+        absx += np.abs(hf[:, k0:k0 + 64]) @ np.abs(Wf)
+    T = oracle.temperature(0, 48, op.t_start, op.t_end)
+    E = K * 2.0 ** -23 * absx.max(axis=1)
+    for i, r in enumerate(rows):
+        b, p = divmod(int(r), L)
+        H, A, Y, gap = oracle.row(x64[i], T, True, 0, b, p, 0)
+        assert abs(g["entropy"][b, p] - H) <= H_TOL, (r, g["entropy"][b, p], H)
+        top2 = np.sort(x64[i])[-2:]
+        if top2[1] - top2[0] >= 2 * E[i]:
+            assert g["argmax"][b, p] == A, r
+        if gap >= max(1e-6, 2 * E[i] / T):
+            assert g["sampled"][b, p] == Y, r
+    # selection from the GPU's own entropies: exactly the k lowest (H, p) masked positions
+    for b in range(B):
+        Hb = g["entropy"][b].astype(np.float64)
+        order = np.lexsort((np.arange(L), Hb))
+        before = np.concatenate([[0.0], np.cumsum(Hb[order])[:-1]])
+        if np.min(np.abs(before[1:] - float(np.float32(0.1)))) < 1e-5:
+            continue
+        k = int(np.sum((np.arange(L) == 0) | (before <= float(np.float32(0.1)))))
+        assert sorted(np.nonzero(g["selected"][b])[0].tolist()) == sorted(order[:k].tolist())
+
+
+def test_unembed_rejects_bad_shapes():
+    gp, _ = params_pair()
+    c = eb.Canvas(1, 16, 64, eb.EB_BF16)
+    h = torch.zeros((16, 12), dtype=torch.int16, device="cuda")
+    W = torch.zeros((12, 64), dtype=torch.int16, device="cuda")
+    with pytest.raises(eb.EbError) as ei:
+        c.unembed_step(gp, h, W, 12, 0, 0.8)     # K not a multiple of 8
+    assert ei.value.status == eb.EB_ERR_INVALID
+    h2 = torch.zeros((16, 16), dtype=torch.int16, device="cuda")
+    W2 = torch.zeros((16, 60), dtype=torch.int16, device="cuda")
+    c2 = eb.Canvas(1, 16, 60, eb.EB_BF16)
+    with pytest.raises(eb.EbError) as ei:
+        c2.unembed_step(gp, h2, W2, 16, 0, 0.8)  # V not a multiple of 8
+    assert ei.value.status == eb.EB_ERR_INVALID

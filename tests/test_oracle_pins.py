@@ -327,3 +327,38 @@ def test_unselected_positions_are_remasked():
     sel = r.selected[0].astype(bool)
     assert (st.tokens[0][~sel] == -1).all() and (st.mask[0][~sel] == 1).all()
     assert (st.tokens[0][sel] == r.Y[0][sel]).all()
+
+
+# ---------------------------------------------------------------- unembedding product
+
+def test_unembed_logits_one_hot_rows_and_brute_force():
+    from eb_synth import to_bf16_bits
+    rng = np.random.default_rng(21)
+    K, V = 24, 40
+    W = to_bf16_bits(rng.standard_normal((K, V)).astype(np.float32) * 0.5)
+    Wf = oracle.bf16_to_f64(W)
+    # a one-hot hidden state selects one row of W exactly
+    h = np.zeros((3, K), np.float32)
+    h[0, 5] = 1.0
+    h[1, 0] = 1.0
+    h[2, K - 1] = -2.0
+    out = oracle.unembed_logits(to_bf16_bits(h), W)
+    assert np.array_equal(out[0], Wf[5]) and np.array_equal(out[1], Wf[0])
+    assert np.array_equal(out[2], -2.0 * Wf[K - 1])
+    # brute-force triple loop on random bf16 inputs
+    hb = to_bf16_bits(rng.standard_normal((4, K)).astype(np.float32))
+    hf = oracle.bf16_to_f64(hb)
+    got = oracle.unembed_logits(hb, W)
+    for m in range(4):
+        for v in range(V):
+            ref = 0.0
+            for k in range(K):
+                ref += hf[m, k] * Wf[k, v]
+            assert abs(got[m, v] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_bf16_to_f64_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x0000, 0x4049, 0x7F7F], np.uint16)
+    vals = oracle.bf16_to_f64(bits)
+    assert vals[0] == 1.0 and vals[1] == -1.0 and vals[2] == 0.0
+    assert vals[3] == 3.140625 and vals[4] == float(np.float32(3.3895313892515355e38))

@@ -21,7 +21,8 @@ EB_STATUS_NONFINITE = 0x100
 
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",
-            "eb_unembed_workspace_bytes", "eb_unembed_sample", "eb_unembed_logits")
+            "eb_unembed_workspace_bytes", "eb_unembed_sample", "eb_unembed_logits",
+            "eb_sampler_step_noalloc")
 
 
 class EbParams(ctypes.Structure):
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
     L.eb_unembed_sample.restype = i32
     L.eb_unembed_logits.argtypes = [i32, i32, i32, P, P, P, P]
     L.eb_unembed_logits.restype = i32
+    L.eb_sampler_step_noalloc.argtypes = ([ctypes.POINTER(EbParams), i32, i32, i32, i32, P, i32,
+                                           ctypes.c_float] + [P] * 11 + [P])
+    L.eb_sampler_step_noalloc.restype = i32
     _lib = L
     return L
 
@@ -152,6 +156,20 @@ def eb_sample_canvas(params: EbParams, B: int, L: int, V: int, dtype: int, logit
                                   _ptr(workspace), workspace_bytes, poll_every,
                                   ctypes.byref(ran), _stream(stream)))
     return ran.value
+
+
+def eb_sampler_step_noalloc(params: EbParams, B: int, L: int, V: int, dtype: int, logits,
+                            step: int, temperature: float, mask, tokens, prev_argmax, status,
+                            steps_taken, entropy, argmax, sampled, selected, committed,
+                            mean_entropy, stream=None) -> None:
+    """eb_sampler_step with the library's fixed scratch instead of a caller workspace (for
+    callers that cannot allocate device memory; B * L <= 8192, calls must not overlap)."""
+    _check(lib().eb_sampler_step_noalloc(ctypes.byref(params), B, L, V, dtype, _ptr(logits), step,
+                                         float(temperature), _ptr(mask), _ptr(tokens),
+                                         _ptr(prev_argmax), _ptr(status), _ptr(steps_taken),
+                                         _ptr(entropy), _ptr(argmax), _ptr(sampled),
+                                         _ptr(selected), _ptr(committed), _ptr(mean_entropy),
+                                         _stream(stream)))
 
 
 def eb_unembed_workspace_bytes(B: int, L: int, K: int, V: int) -> int:

@@ -1113,6 +1113,78 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
     return st == EB_OK ? ok() : st;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- fixed-scratch variant
+//
+// Scratch of eb_sampler_step_noalloc: a file-scope device array sized for at most
+// EB_NOALLOC_MAX_ROWS canvas positions (B * L).  Every device that loads this library holds
+// it until the process exits.  Host code cannot use the array's name as a device address,
+// so its address is looked up once per device with cudaGetSymbolAddress and cached.
+namespace {
+
+constexpr long long kNoallocRows = EB_NOALLOC_MAX_ROWS;
+constexpr size_t kNoallocBytes = ((size_t)(kNoallocRows + ebk::kMaxGrid) * sizeof(ebk::Partial) + 255) / 256 * 256 +
+                                 ((size_t)(kNoallocRows + 1) * sizeof(uint32_t) + 255) / 256 * 256;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+namespace {
+
+struct NoallocScratch {
+    std::atomic<int> ready{0};
+    void *ptr = nullptr;
+};
+NoallocScratch g_noalloc[64];
+
+// Device address of the array on the current device (set up on the first call per device).
+eb_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(EB_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= 64) return fail(EB_ERR_UNSUPPORTED, "device index %d >= 64", dev);
+    NoallocScratch &g = g_noalloc[dev];
+    if (g.ready.load(std::memory_order_acquire) == 0) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(EB_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch: %s", cudaGetErrorString(e));
+        g.ptr = p;
+        g.ready.store(1, std::memory_order_release);
+    }
+    *out = g.ptr;
+    return EB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+eb_status eb_sampler_step_noalloc(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                                  const void *d_logits, int step, float temperature,
+                                  uint8_t *d_mask, int32_t *d_tokens, int32_t *d_prev_argmax,
+                                  int32_t *d_status, int32_t *d_steps_taken,
+                                  float *d_entropy, int32_t *d_argmax, int32_t *d_sampled,
+                                  uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
+                                  void *stream)
+{
+    if (B > 0 && L > 0 && (long long)B * L > kNoallocRows)
+        return fail(EB_ERR_UNSUPPORTED, "B*L = %lld exceeds the fixed scratch of %lld positions; use "
+                    "eb_sampler_step with a caller-allocated workspace", (long long)B * L, kNoallocRows);
+    void *scratch = nullptr;
+    if (B > 0) {
+        const eb_status st = noalloc_scratch(&scratch);
+        if (st != EB_OK) return st;
+        if (eb_workspace_bytes(B, L, V, dtype) > kNoallocBytes)
+            return fail(EB_ERR_UNSUPPORTED, "the fixed scratch is too small for this call");
+    }
+    return eb_sampler_step(params, B, L, V, dtype, d_logits, step, temperature, d_mask, d_tokens,
+                           d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax, d_sampled,
+                           d_selected, d_committed, d_mean_entropy, scratch, kNoallocBytes, stream);
+}
+
 eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtype dtype,
                            eb_logits_fn logits_fn, void *user, void *d_logits, int start_step,
                            uint8_t *d_mask, int32_t *d_tokens, int32_t *d_prev_argmax,

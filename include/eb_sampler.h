@@ -122,6 +122,41 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
                           uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
                           void *d_workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * eb_sampler_step without a workspace argument.  There is no counterpart in the pages: this
+ * entry point exists for callers that cannot call cudaMalloc.  For example:
+ *   - a host process whose device memory is all reserved up front by its own pool, so that a
+ *     further allocation would fail;
+ *   - a plugin that runs inside someone else's runtime, where only that runtime may allocate;
+ *   - a latency-critical loop where the implicit synchronisation of an allocation is not
+ *     acceptable.
+ * The per-row partial states live instead in one fixed array of device memory inside this
+ * library, sized for at most EB_NOALLOC_MAX_ROWS canvas positions (B * L).  That is 557,312
+ * bytes, and every device that loads the library holds them until the process exits.
+ *
+ * Arguments, results and errors are those of eb_sampler_step, with the workspace supplied by
+ * the library.  B * L above EB_NOALLOC_MAX_ROWS returns EB_ERR_UNSUPPORTED and launches
+ * nothing.  The call allocates no memory, neither itself nor through a library.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current, and caches it.  Make that first call before any stream capture.
+ *
+ * All calls share the one array, and it keeps whatever the last call left in it.  Nothing in
+ * it needs to start at zero: each call overwrites what it reads later.  Two calls whose work
+ * overlaps on the GPU (different streams, or different host threads without ordering) race on
+ * the array and may return wrong results.  Order them on one stream, or use eb_sampler_step
+ * with separate workspaces.
+ */
+#define EB_NOALLOC_MAX_ROWS 8192
+
+eb_status eb_sampler_step_noalloc(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                                  const void *d_logits, int step, float temperature,
+                                  uint8_t *d_mask, int32_t *d_tokens, int32_t *d_prev_argmax,
+                                  int32_t *d_status, int32_t *d_steps_taken,
+                                  float *d_entropy, int32_t *d_argmax, int32_t *d_sampled,
+                                  uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
+                                  void *stream);
+
 /* Logits provider of the denoising loop: enqueue, on `stream`, the logits of `step`
  * into d_logits [B, L, V] (the denoiser).  It may read d_tokens / d_status (device) to
  * condition on the canvas and to skip halted canvases.  Returns 0 on success. */

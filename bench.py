@@ -274,8 +274,16 @@ def run_ours(args, rank, world, local):
         bufs.append(x)
     masks = workload_masks()
     K, W = args.steps, args.warmup
-    pool = state_pool(W + K, masks, device)
-    ptrs = [state_ptrs(pool, i) for i in range(W + K)]
+    # the timed steps run as replays of a CUDA graph of N steps (N divides K), so the host's
+    # per-call cost stays out of the device time; each replay first restores its N canvas
+    # states from a pristine copy, so every step does the workload's work
+    N = max(d for d in range(1, min(K, 200) + 1) if K % d == 0)
+    R = K // N
+    pool = state_pool(N, masks, device)
+    pristine = {k: v.clone() for k, v in pool.items()}
+    ptrs = [state_ptrs(pool, i) for i in range(N)]
+    wpool = state_pool(W, masks, device)
+    wptrs = [state_ptrs(wpool, i) for i in range(W)]
     ws_bytes = eb.eb_workspace_bytes(B, L, V, eb.EB_BF16)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     params = eb.eb_default_params(seed=0)
@@ -284,24 +292,39 @@ def run_ours(args, rank, world, local):
     wsp = ws.data_ptr()
     step_fn = lib.eb_sampler_step
 
-    def one(i):
-        st = step_fn(pref, B, L, V, eb.EB_BF16, buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *ptrs[i],
-                     wsp, ws_bytes, sp)
+    def one(i, sptrs, stream_ptr):
+        st = step_fn(pref, B, L, V, eb.EB_BF16, buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *sptrs[i],
+                     wsp, ws_bytes, stream_ptr)
         if st != 0:
             raise eb.EbError(st, lib.eb_last_error().decode())
 
     for i in range(W):
-        one(i)
+        one(i, wptrs, sp)
     torch.cuda.synchronize()
 
-    k1b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    k1e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k1b = [torch.cuda.Event(enable_timing=True) for _ in range(N)]
+    k1e = [torch.cuda.Event(enable_timing=True) for _ in range(N)]
     for e in k1b + k1e:
-        e.record(stream)          # materialise the CUDA events before timing
+        e.record(stream)          # materialise the CUDA events before capture
     torch.cuda.synchronize()
     evb = [e.cuda_event for e in k1b]
     eve = [e.cuda_event for e in k1e]
     set_prof = lib.eb_set_profile_events
+
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        graph.capture_begin()
+        for k in pool:
+            pool[k].copy_(pristine[k])
+        csp = torch.cuda.current_stream(device).cuda_stream
+        for j in range(N):
+            set_prof(evb[j], eve[j])
+            one(j, ptrs, csp)
+        graph.capture_end()
+    torch.cuda.synchronize()
+    graph.replay()                # one untimed replay after capture
+    torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
 
@@ -309,19 +332,18 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         start.record(stream)
-        for j in range(K):
-            set_prof(evb[j], eve[j])
-            one(W + j)
+        for _ in range(R):
+            graph.replay()
         end.record(stream)
         torch.cuda.synchronize()
     barrier(dist, local)
     elapsed = start.elapsed_time(end) / 1e3
-    k1_ms = [b.elapsed_time(e) for b, e in zip(k1b, k1e)]
+    k1_ms = [b.elapsed_time(e) for b, e in zip(k1b, k1e)]     # the last replay's N launches
     value, slowest = aggregate(K, elapsed, world, dist, local)
 
     # every timed step did the workload's work: running canvas, one position committed
-    st = pool["status"][W:].cpu().numpy()
-    com = pool["committed"][W:].cpu().numpy()
+    st = pool["status"].cpu().numpy()
+    com = pool["committed"].cpu().numpy()
     if not ((st == 0).all() and (com >= 1).all()):
         raise RuntimeError("timed steps did not run the expected workload")
 
@@ -349,6 +371,7 @@ def run_ours(args, rank, world, local):
             "workload": WORKLOAD,
             "B": B, "L": L, "V": V, "logits_dtype": "bf16", "masked": 128, "temperature": TEMPERATURE,
             "l2": "10 rotating 128 MiB logit buffers (1.25 GiB > 126 MB L2)",
+            "launch": f"CUDA graph of {N} steps (+ one canvas-state restore) replayed {R} times",
             "parallelism": f"replicas x{world}",
         },
         "hbm_gbs_step": BYTES_PER_STEP * K / elapsed / 1e9,
@@ -367,7 +390,7 @@ def run_ours(args, rank, world, local):
             "bytes_per_launch": BYTES_PER_STEP,
         },
         "e2e": e2e,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K,                 # row statistics + selection per step
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

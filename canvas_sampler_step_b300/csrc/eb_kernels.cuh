@@ -7,23 +7,27 @@
 // k1_rowstats (one launch per step) streams the [B, L, V] logits exactly once.
 //   * Work split.  Row r of a running canvas weighs nvec * w (w = w_masked for masked rows,
 //     which also draw Gumbel noise, w_unmasked otherwise; rows of halted canvases weigh 0).
-//     The prefix sums P of the weights are cut into G equal ranges, one per CTA (G = one CTA
-//     per SM), so CTAs finish together even though masked rows cost more instructions per
-//     byte, and halted canvases cost nothing.  CTA c writes one partial state for every row
-//     its range touches to slot (row + c) of the workspace (the (row, CTA) pairs form a
-//     staircase, so row + c is unique).
-//   * Data movement.  One producer warp moves the CTA's rows through a ring of 16 KiB
-//     shared-memory stages with 1-D TMA bulk copies (cp.async.bulk ... mbarrier::complete_tx);
-//     16 consumer warps read 16-byte vectors from shared memory.  Every mbarrier wait is
-//     bounded; a CTA whose wait gives up marks its partials and returns.
+//     The prefix sums P of the weights are cut into G equal ranges, one per warp (16 warps per
+//     CTA, one CTA per SM), so warps finish together even though masked rows cost more
+//     instructions per byte, and halted canvases cost nothing.  Warp g writes one partial
+//     state for every row its range touches to slot (row + g) of the workspace (the (row,
+//     warp) pairs form a staircase, so row + g is unique).
+//   * Data movement.  Each warp streams its row segments with coalesced 16-byte loads that
+//     bypass L1 (ld.global.nc.L1::no_allocate), two vectors per lane per batch, the next batch
+//     in flight while the current one is consumed; whole batches run without bounds checks.
+//     (A TMA bulk-copy ring with a producer warp measured slower on this workload: 81.7 us
+//     against 71-79 us, its consumers idling on the ring's barriers.)
 //   * Per element: t = x * log2(e)/T - xm * log2(e)/T, e = 2^t (MUFU), S += e, T2 += t e,
 //     with xm the running maximum of the thread's raw logits (first index kept for the
-//     argmax).  H = ln 2 (log2 S - T2 / S) after merging.
+//     argmax); the FMAs and adds run on packed f32x2 pairs.  H = ln 2 (log2 S - T2 / S)
+//     after merging.  A new running maximum is handled behind a warp vote so that the rare
+//     rescale stays a branch.
 //   * Gumbel-max for masked rows: with u from a Philox4x32-10 word and E = -ln u, the sample
 //     maximises z - ln E.  Since E >= 1 - u, an entry can beat the best score so far only if
 //     1 - u < 2^t K, K = 2^(xm log2e / T - best log2e); that test is one LOP3, one FFMA and
 //     one predicate-or per entry.  Entries that pass it (a handful per warp and row) take the
-//     exact score z - logf(-log1pf(-(1 - u))); the warp shares its best score when it moves.
+//     exact score z - logf(-log1pf(-(1 - u))) in an out-of-line function; the warp shares its
+//     best score when it moves.
 // k2_select (one CTA per canvas) merges each row's partials in ascending CTA order
 // (deterministic), runs the stop test, the entropy-bounded selection and the commit /
 // re-mask / finalisation.  Sums of entropies are exact 64-bit fixed point (2^-40 nats).
@@ -40,16 +44,12 @@ namespace ebk {
 // ---------------------------------------------------------------- launch geometry
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kK1Threads = kConsumers + 32;        // + one producer warp
-constexpr int kVecPerStage = 1024;                  // 16-byte vectors per ring stage
-constexpr int kStageBytes = kVecPerStage * 16;
-constexpr int kStages = 10;
 constexpr int kMaxWeightedRows = 4096;
 constexpr int kK2Threads = 256;
 constexpr int kMaxL = 1024;
 constexpr int kMaxGrid = 8192;
-constexpr int kWeightUnmasked = 4;
-constexpr int kWeightMasked = 10;
+constexpr int kWeightUnmasked = 6;                 // relative cost of a vector of an unmasked row
+constexpr int kWeightMasked = 13;                  // ... and of a masked row (measured 2.16 : 1)
 constexpr uint32_t kWaitLimit = 1u << 26;           // mbarrier polls before giving up
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -94,6 +94,7 @@ struct K1Args {
     const int32_t *status;
     Partial *partials;
     uint32_t *prefix_out;   // [rows + 1] weight prefix (weighted mode; written by CTA 0)
+    int2 *rowunits;         // [rows]: first and last partition unit of each row (written here)
     long long nvec_row;     // 16-byte vectors per row (elements per row on the scalar path)
     long long row_bytes;
     int rows;
@@ -109,6 +110,7 @@ struct K1Args {
 struct K2Args {
     const Partial *partials;
     const uint32_t *prefix;  // weighted mode: [rows + 1]
+    const int2 *rowunits;    // [rows]: first and last partition unit of each row
     uint8_t *mask;
     int32_t *tokens;
     int32_t *prev_argmax;
@@ -151,6 +153,50 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c)
+{
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed pairs of binary32 values in one 64-bit register (Blackwell f32x2 arithmetic: one
+// instruction per two lanes' worth of FADD / FFMA / FMUL).
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk2(float lo, float hi)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void upk2(f32x2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 // Philox4x32-10 (Salmon et al., SC'11): per round two 32x32->64 products of counter words 0
@@ -246,6 +292,247 @@ __device__ __forceinline__ void warp_best(float &best, int &bi)
 __device__ __forceinline__ RowState empty_state()
 {
     return RowState{kEmptyMax, 0.0f, 0.0f, 0x7FFFFFFF, -INFINITY, -1};
+}
+
+// ---------------------------------------------------------------- packed per-vector body
+
+// Sums of one consumer thread over its part of a row, as two packed pairs each (four
+// independent accumulation chains): S = sum 2^t, T2 = sum t 2^t.
+struct PackedSums {
+    f32x2 S0, S1, T0, T1;
+};
+
+__device__ __forceinline__ void packed_zero(PackedSums &q)
+{
+    q.S0 = q.S1 = q.T0 = q.T1 = 0ull;       // +0.0f in both halves
+}
+
+// New running maximum: every accumulator is rescaled by sc = 2^d (d <= 0).  A weight that
+// underflows to 0 drops the old sums even if they overflowed.
+__device__ __forceinline__ void packed_rescale(PackedSums &q, float d, float sc)
+{
+    if (sc == 0.0f) {
+        packed_zero(q);
+        return;
+    }
+    const f32x2 d2 = pk2(d, d), sc2 = pk2(sc, sc);
+    q.T0 = mul2(sc2, fma2(d2, q.S0, q.T0));
+    q.T1 = mul2(sc2, fma2(d2, q.S1, q.T1));
+    q.S0 = mul2(q.S0, sc2);
+    q.S1 = mul2(q.S1, sc2);
+}
+
+__device__ __forceinline__ void packed_fold(const PackedSums &q, RowState &st)
+{
+    float a, b, c, d;
+    upk2(add2(q.S0, q.S1), a, b);
+    upk2(add2(q.T0, q.T1), c, d);
+    st.S = a + b;
+    st.T2 = c + d;
+}
+
+// Philox4x32-10 with the round keys derived in place from the seed words (k0, k1).
+__device__ __forceinline__ uint4 philox_seed(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                             uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+struct GumbelBest {
+    float score;
+    int idx;
+};
+
+// The rare exact pass over a group of N logits (entries v0 ..) whose group test passed: every
+// entry with 1 - u < 2^t K takes the exact score z - ln(-ln u), and the best one so far is
+// returned.  Kept out of line so that the unrolled hot loop stays small; it recomputes the
+// uniforms and 2^t from the logits.
+template <int N>
+__device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint32_t v0, float c, float invT,
+                                                      float nb, float K, uint32_t p, uint32_t step,
+                                                      uint32_t sw, uint32_t k0, uint32_t k1, GumbelBest best)
+{
+    const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    uint32_t w[8];
+    const uint4 u0 = philox_seed(v0 >> 2, p, step, sw, k0, k1);
+    w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+    if (N == 8) {
+        const uint4 u1 = philox_seed((v0 >> 2) + 1, p, step, sw, k0, k1);
+        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float e = ex2(fmaf(x[j], c, nb));
+        const float f = one_minus_u_plus(w[j]);
+        if (f < fmaf(e, K, kCandAdd)) {
+            const float delta = f - kOneMinusHalfUlp;          // 1 - u, exact
+            const float E = -log1pf(-delta);                   // -ln u
+            const float score = x[j] * invT - logf(E);
+            const int idx = (int)(v0 + (uint32_t)j);
+            if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
+        }
+    }
+    return best;
+}
+
+// N = 8 or 4 consecutive logits x of a canvas row, entries v0 .. v0+N-1 (v0 a multiple of
+// N): running max / first argmax, S and T2 (on packed f32x2 pairs when EB_PACKED is 1), and
+// for masked rows the Gumbel candidate test, done once per group: the smallest 1 - u of its
+// entries against the largest 2^t.  `a` supplies c = log2(e)/T, invT = 1/T, the step and the
+// Philox round keys.  WARP_ROW: the 32 lanes work on the same row (they share the best score
+// when it moves, so every lane must call this with the same trip count; `valid` masks lanes
+// without a group); otherwise every lane owns its row.
+#ifndef EB_PACKED
+#define EB_PACKED 1
+#endif
+#ifndef EB_GROUP_TEST
+#define EB_GROUP_TEST 0
+#endif
+template <int N, bool MASKED, bool WARP_ROW, typename Args>
+__device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, uint32_t v0, const Args &a,
+                                             uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                             PackedSums &q, float &nb, f32x2 &nb2, float &K)
+{
+    float vmax = 0.0f;
+    float e[N];
+    if (valid) {
+        if constexpr (N == 8) vmax = max3(max3(x[0], x[1], x[2]), max3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+        else vmax = max3(x[0], x[1], fmaxf(x[2], x[3]));
+    }
+    // a new running maximum is rare after the first groups; the vote keeps this a real branch
+    // (the compiler would otherwise predicate the whole block into every group)
+    const bool newmax = valid && vmax > st.xm;
+    if (__any_sync(WARP_ROW ? 0xFFFFFFFFu : __activemask(), newmax)) {
+        if (newmax) {
+                const float d = (st.xm - vmax) * a.c;
+                packed_rescale(q, d, ex2(d));
+                int j0 = N - 1;
+#pragma unroll
+                for (int j = N - 1; j >= 0; --j)
+                    if (x[j] == vmax) j0 = j;
+                st.ai = (int)(v0 + (uint32_t)j0);
+                st.xm = vmax;
+                nb = -vmax * a.c;
+                nb2 = pk2(nb, nb);
+            if (MASKED) K = cand_scale(st.xm, st.best, a.c);
+        }
+    }
+    if (valid) {
+#if EB_PACKED
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const f32x2 tp = fma2(pk2(x[2 * i], x[2 * i + 1]), c2, nb2);
+            float t0, t1;
+            upk2(tp, t0, t1);
+            e[2 * i] = ex2(t0);
+            e[2 * i + 1] = ex2(t1);
+            const f32x2 ep = pk2(e[2 * i], e[2 * i + 1]);
+            if (i & 1) {
+                q.S1 = add2(q.S1, ep);
+                q.T1 = fma2(tp, ep, q.T1);
+            } else {
+                q.S0 = add2(q.S0, ep);
+                q.T0 = fma2(tp, ep, q.T0);
+            }
+        }
+#else
+        // scalar accumulation into the four lanes of the packed sums (S0.lo, S0.hi, S1.lo, S1.hi)
+        float s[4], t2[4];
+        upk2(q.S0, s[0], s[1]);
+        upk2(q.S1, s[2], s[3]);
+        upk2(q.T0, t2[0], t2[1]);
+        upk2(q.T1, t2[2], t2[3]);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            const float t = fmaf(x[j], a.c, nb);
+            e[j] = ex2(t);
+            s[j & 3] += e[j];
+            t2[j & 3] = fmaf(t, e[j], t2[j & 3]);
+        }
+        q.S0 = pk2(s[0], s[1]);
+        q.S1 = pk2(s[2], s[3]);
+        q.T0 = pk2(t2[0], t2[1]);
+        q.T1 = pk2(t2[2], t2[3]);
+#endif
+    }
+    if constexpr (MASKED) {
+        bool cand = false;
+        if (valid) {
+            const uint4 u0 = philox(v0 >> 2, p, (uint32_t)a.step, sw, a.keys);
+#if EB_GROUP_TEST
+            float fmin = min3(one_minus_u_plus(u0.x), one_minus_u_plus(u0.y),
+                              fminf(one_minus_u_plus(u0.z), one_minus_u_plus(u0.w)));
+            if constexpr (N == 8) {
+                const uint4 u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
+                fmin = min3(fmin, min3(one_minus_u_plus(u1.x), one_minus_u_plus(u1.y), one_minus_u_plus(u1.z)),
+                            one_minus_u_plus(u1.w));
+            }
+            // 2^t is largest at the group's maximum: one test bounds all N entries
+            const float emax = ex2(fmaf(vmax, a.c, nb));
+            cand = fmin < fmaf(emax, K, kCandAdd);
+#else
+            uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, 0u, 0u, 0u, 0u};
+            if constexpr (N == 8) {
+                const uint4 u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
+                w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+            }
+#pragma unroll
+            for (int j = 0; j < N; ++j) cand |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
+#endif
+        }
+        const bool go = __any_sync(WARP_ROW ? 0xFFFFFFFFu : __activemask(), cand);
+        if (go) {
+            if (cand) {
+                const float4 xa = make_float4(x[0], x[1], x[2], x[3]);
+                const float4 xb = N == 8 ? make_float4(x[N > 4 ? 4 : 0], x[N > 5 ? 5 : 0], x[N > 6 ? 6 : 0],
+                                                       x[N > 7 ? 7 : 0])
+                                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                const GumbelBest g = gumbel_exact_group<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
+                                                           a.keys.k[0], a.keys.k[1],
+                                                           GumbelBest{st.best, st.bi});
+                st.best = g.score;
+                st.bi = g.idx;
+            }
+            if (WARP_ROW) warp_best(st.best, st.bi);
+            K = cand_scale(st.xm, st.best, a.c);
+        }
+    }
+}
+
+// One 16-byte vector of VEC logits (8 bf16 or 4 fp32) of a row, entries jvec*VEC ..
+template <int VEC, bool MASKED>
+__device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32_t jvec, const K1Args &a,
+                                               uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                               PackedSums &q, float &nb, f32x2 &nb2, float &K)
+{
+    float x[VEC];
+    if constexpr (VEC == 8) {
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w4[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(r.x);
+        x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z);
+        x[3] = __uint_as_float(r.w);
+    }
+    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, p, sw, c2, st, q, nb, nb2, K);
 }
 
 // ---------------------------------------------------------------- mbarrier / bulk copy PTX
@@ -347,7 +634,9 @@ struct SegmentCursor {
         hi = (unsigned long long)(cta + 1) * W / (unsigned long long)G;
         r = (lo < hi) ? p.first_row_after(lo) : p.rows;
     }
-    // next segment; false when done.  Rows of zero weight are skipped.
+    // next segment; false when done.  Rows of zero weight are skipped.  `first` / `last`: the
+    // segment starts / ends the row's weight range (so this unit is the row's first / last).
+    bool first = false, last = false;
     __device__ __forceinline__ bool next(int &row, long long &j0, long long &j1)
     {
         while (r < part.rows) {
@@ -366,6 +655,8 @@ struct SegmentCursor {
             j1 = (long long)((s1 + wv - 1) / wv);
             if (j1 > part.nvec) j1 = part.nvec;
             if (j0 > j1) j0 = j1;
+            first = a >= lo;       // this unit holds the row's first weight unit
+            last = b <= hi;        // ... and its last one
             return true;
         }
         return false;

@@ -180,17 +180,6 @@ __device__ void build_prefix(const K1Args &a, uint32_t *P, uint8_t *mflag, uint3
     __syncthreads();
 }
 
-struct K1Smem {
-    static constexpr size_t ring = 0;
-    static constexpr size_t full = ring + (size_t)kStages * kStageBytes;
-    static constexpr size_t empty = full + (size_t)kStages * 8;
-    static constexpr size_t prefix = empty + (size_t)kStages * 8;
-    static constexpr size_t mflag = prefix + (size_t)(kMaxWeightedRows + 1) * 4;
-    static constexpr size_t red = (mflag + kMaxWeightedRows + 15) / 16 * 16;
-    static constexpr size_t scan = red + (size_t)kConsumerWarps * sizeof(RowState);
-    static constexpr size_t total = scan + 32 * 4;
-};
-
 __device__ __forceinline__ void write_partial(Partial *dst, const RowState &s, int flags)
 {
     Partial out;
@@ -227,110 +216,123 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, R
     consumer_sync();
 }
 
-// TMA path: rows start 16-byte aligned and hold whole 16-byte vectors.
-template <int KIND>
-__global__ void __launch_bounds__(kK1Threads, 1) k1_rowstats_tma(const K1Args a)
+// ------------------------------------------------------------------ direct-load path
+//
+// The same row statistics without the shared-memory ring: every warp is one unit of the
+// weighted partition (its slot is row + global warp index) and streams its row segments with
+// 16-byte loads that bypass L1, U vectors per lane per batch, the next batch in flight while
+// the current one is consumed.  Warps merge their lanes with shuffles; no block barrier runs
+// after the prefix is built.
+constexpr int kDirectThreads = 512;
+constexpr int kDirectWarps = kDirectThreads / 32;
+constexpr int kDirectU = 2;             // vectors per lane per batch (two batches in flight)
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <int U>
+__device__ __forceinline__ void load_full(uint4 (&r)[U], const uint4 *src, uint32_t jb, uint32_t lane)
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = ld_stream(src + jb + lane + 32u * (uint32_t)u);
+}
+
+template <int VEC, bool MASKED, int U>
+__device__ __forceinline__ void consume_full(const uint4 (&r)[U], uint32_t jb, uint32_t lane, const K1Args &a,
+                                             uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                             float &nb, f32x2 &nb2, float &K)
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        consume_packed<VEC, MASKED>(r[u], true, jb + lane + 32u * (uint32_t)u, a, p, sw, c2, st, q, nb, nb2, K);
+}
+
+// One row segment [j0, j1) of a warp: whole batches of 32 U vectors run without bounds
+// checks from two register buffers (the next batch loads while the current one is consumed),
+// the remainder with checks.
+template <int VEC, bool MASKED, int U>
+__device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
+                                               uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                               PackedSums &q)
+{
+    constexpr uint32_t kBatch = 32u * U;
+    const uint32_t lane = threadIdx.x & 31;
+    float nb = -st.xm * a.c;
+    f32x2 nb2 = pk2(nb, nb);
+    float K = cand_scale(st.xm, st.best, a.c);
+    const uint32_t jf = j0 + (j1 - j0) / kBatch * kBatch;
+    if (jf > j0) {
+        uint4 A[U], B[U];
+        load_full<U>(A, src, j0, lane);
+        for (uint32_t jb = j0;; jb += 2 * kBatch) {
+            const bool hasB = jb + kBatch < jf;
+            if (hasB) load_full<U>(B, src, jb + kBatch, lane);
+            consume_full<VEC, MASKED, U>(A, jb, lane, a, p, sw, c2, st, q, nb, nb2, K);
+            if (!hasB) break;
+            const bool hasA = jb + 2 * kBatch < jf;
+            if (hasA) load_full<U>(A, src, jb + 2 * kBatch, lane);
+            consume_full<VEC, MASKED, U>(B, jb + kBatch, lane, a, p, sw, c2, st, q, nb, nb2, K);
+            if (!hasA) break;
+        }
+    }
+#pragma unroll 1
+    for (uint32_t jb = jf; jb < j1; jb += 32u) {
+        const uint32_t idx = jb + lane;
+        const bool valid = idx < j1;
+        const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+        consume_packed<VEC, MASKED>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K);
+    }
+}
+
+template <int KIND, int U>
+__global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1Args a)
 {
     using Tr = KindTraits<KIND>;
     constexpr int VEC = Tr::VEC;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char *ring = smem + K1Smem::ring;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + K1Smem::full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + K1Smem::empty);
-    uint32_t *P = reinterpret_cast<uint32_t *>(smem + K1Smem::prefix);
-    uint8_t *mflag = smem + K1Smem::mflag;
-    RowState *red = reinterpret_cast<RowState *>(smem + K1Smem::red);
-    uint32_t *scan = reinterpret_cast<uint32_t *>(smem + K1Smem::scan);
-
+    __shared__ uint32_t P[kMaxWeightedRows + 1];
+    __shared__ uint8_t mflag[kMaxWeightedRows];
+    __shared__ uint32_t scan[32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the dependent selection grid may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
     if (a.weighted) build_prefix(a, P, mflag, scan);
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
     __syncthreads();
     if (a.weighted && blockIdx.x == 0)
         for (int r = tid; r <= a.rows; r += blockDim.x) a.prefix_out[r] = P[r];
-
+    const int gw = blockIdx.x * kDirectWarps + warp;
     const Partition part{P, a.nvec_row, a.rows, a.weighted};
     SegmentCursor cur;
-    cur.begin(part, blockIdx.x, a.G);
+    cur.begin(part, gw, a.G);
+    const f32x2 c2 = pk2(a.c, a.c);
     int row;
     long long j0, j1;
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        if (lane != 0) return;
-        uint32_t s = 0;
-        bool ok = true;
-        while (ok && cur.next(row, j0, j1)) {
-            if (!a.weighted && a.status[row / a.L] != EB_RUNNING) continue;
-            const char *src = static_cast<const char *>(a.logits) + (size_t)row * (size_t)a.row_bytes;
-            for (long long j = j0; j < j1; j += kVecPerStage) {
-                const uint32_t n = (uint32_t)min((long long)kVecPerStage, j1 - j);
-                const int slot = (int)(s % kStages);
-                if (s >= (uint32_t)kStages && !mbar_wait(&empty[slot], ((s / kStages) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[slot], n * 16u);
-                bulk_g2s(ring + (size_t)slot * kStageBytes, src + j * 16, n * 16u, &full[slot]);
-                ++s;
-            }
-        }
-        // every issued copy has landed before this thread leaves
-        const uint32_t first = s > (uint32_t)kStages ? s - kStages : 0;
-        for (uint32_t q = first; q < s; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1);
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    uint32_t s = 0;
-    bool ok = true;
     while (cur.next(row, j0, j1)) {
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
         const uint32_t p = (uint32_t)(row - b * a.L);
         const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
         const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.logits) +
+                                                           (size_t)row * (size_t)a.row_bytes);
         RowState st = empty_state();
-        float nb = -st.xm * a.c;
-        float K = cand_scale(st.xm, st.best, a.c);
-        for (long long j = j0; ok && j < j1; j += kVecPerStage) {
-            const int n = (int)min((long long)kVecPerStage, j1 - j);
-            const int slot = (int)(s % kStages);
-            if (!mbar_wait(&full[slot], (s / kStages) & 1)) {
-                ok = false;
-                break;
-            }
-            const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (size_t)slot * kStageBytes);
-            if (masked) {
-#pragma unroll
-                for (int k = 0; k < kVecPerStage / kConsumers; ++k) {
-                    const int jj = tid + k * kConsumers;
-                    const bool valid = jj < n;
-                    float x[VEC];
-                    if (valid) Tr::unpack(stage[jj], x);
-                    consume_vec<VEC, true>(x, valid, j + jj, a, p, sw, st, nb, K);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < kVecPerStage / kConsumers; ++k) {
-                    const int jj = tid + k * kConsumers;
-                    const bool valid = jj < n;
-                    float x[VEC];
-                    if (valid) Tr::unpack(stage[jj], x);
-                    consume_vec<VEC, false>(x, valid, j + jj, a, p, sw, st, nb, K);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            ++s;
+        PackedSums q;
+        packed_zero(q);
+        if (masked) direct_segment<VEC, true, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q);
+        else direct_segment<VEC, false, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q);
+        packed_fold(q, st);
+        const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
+        warp_merge(st, a.c);
+        if (lane == 0) {
+            write_partial(&a.partials[row + gw], st, nan_here ? kPartialNonfinite : 0);
+            if (cur.first) a.rowunits[row].x = gw;
+            if (cur.last) a.rowunits[row].y = gw;
         }
-        reduce_and_store(st, a, red, scan, row, ok ? 0 : kPartialTimeout);
     }
 }
 
@@ -343,6 +345,7 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
     __shared__ RowState red[kConsumerWarps];
     __shared__ uint32_t scan[32];
     const int tid = threadIdx.x;
+    asm volatile("griddepcontrol.launch_dependents;");
     if (a.weighted) build_prefix(a, P, mflag, scan);
     __syncthreads();
     if (a.weighted && blockIdx.x == 0)
@@ -374,6 +377,10 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
             else consume_vec<1, false>(x, valid, v, a, p, sw, st, nb, K);
         }
         reduce_and_store(st, a, red, scan, row, 0);
+        if (tid == 0) {
+            if (cur.first) a.rowunits[row].x = blockIdx.x;
+            if (cur.last) a.rowunits[row].y = blockIdx.x;
+        }
     }
 }
 
@@ -439,6 +446,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         small_total = 0;
     }
     const long long rowbase = (long long)b * L;
+    // launched as a programmatic dependent of the row-statistics kernel: everything above
+    // reads only what that kernel does not write; wait for its partials here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const unsigned long long W = k2_row_start(a, a.rows);
     const unsigned long long G = (unsigned long long)a.G;
     __syncthreads();
@@ -462,10 +472,11 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
                 }
             }
         } else if (w1 > w0) {
-            const int c0 = (int)(((w0 + 1) * G - 1) / W);
-            const int c1 = (int)((w1 * G - 1) / W);
-            for (int c = c0; c <= c1; ++c) {
-                if ((unsigned long long)c * W / G >= (unsigned long long)(c + 1) * W / G) continue;
+            // the units that touched row r, recorded by the row-statistics kernel; only when
+            // the total weight is below the unit count can a unit's range be empty
+            const int2 u = a.rowunits[r];
+            for (int c = u.x; c <= u.y; ++c) {
+                if (W < G && (unsigned long long)c * W / G >= (unsigned long long)(c + 1) * W / G) continue;
                 const Partial q = a.partials[r + c];
                 merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
                 flags |= q.flags;
@@ -732,17 +743,10 @@ eb_status geometry(int *grid_out, int kind)
         if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return fail(EB_ERR_CUDA, "cudaDeviceGetAttribute failed");
-        const size_t smem = ebk::K1Smem::total;
-        if ((size_t)smem_optin < smem)
-            return fail(EB_ERR_UNSUPPORTED, "device offers %d B of shared memory per block, need %zu",
-                        smem_optin, smem);
-        if (cudaFuncSetAttribute(ebk::k1_rowstats_tma<ebk::kF32Vec>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-            cudaFuncSetAttribute(ebk::k1_rowstats_tma<ebk::kBF16Vec>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
-        g.grid[ebk::kF32Vec] = resident_ctas(ebk::k1_rowstats_tma<ebk::kF32Vec>, ebk::kK1Threads, smem, nsm);
-        g.grid[ebk::kBF16Vec] = resident_ctas(ebk::k1_rowstats_tma<ebk::kBF16Vec>, ebk::kK1Threads, smem, nsm);
+        (void)smem_optin;
+        // one CTA of kDirectWarps warps per SM; every warp is one unit of the row partition
+        g.grid[ebk::kF32Vec] = nsm * ebk::kDirectWarps;
+        g.grid[ebk::kBF16Vec] = nsm * ebk::kDirectWarps;
         g.grid[ebk::kF32Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kF32Scalar>, ebk::kConsumers, 0, nsm);
         g.grid[ebk::kBF16Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kBF16Scalar>, ebk::kConsumers, 0, nsm);
         g.ready.store(1, std::memory_order_release);
@@ -828,6 +832,16 @@ eb_status encode_bf16_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint
     return EB_OK;
 }
 
+// Records a profiling event on `stream`; inside a stream capture it becomes a real event
+// record node of the graph (so the event can time each replay).
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    return cudaEventRecord(ev, stream);
+}
+
 ebk::RoundKeys round_keys(uint64_t seed)
 {
     ebk::RoundKeys K;
@@ -848,8 +862,16 @@ float schedule_temperature(const eb_params *p, int step)
 }
 
 // Workspace layout: [partials (rows + kMaxGrid) x 32 B][weight prefix (rows + 1) x 4 B].
-size_t partial_bytes(long long rows) { return align256((size_t)(rows + ebk::kMaxGrid) * sizeof(ebk::Partial)); }
-size_t prefix_bytes(long long rows) { return align256((size_t)(rows + 1) * sizeof(uint32_t)); }
+// Workspace layout: [partials (rows + kMaxGrid) x 32 B][weight prefix (rows + 1) x 4 B]
+// [first / last partition unit of each row, rows x 8 B], each part 256-byte aligned.
+constexpr size_t align256c(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr size_t partial_bytes(long long rows) { return align256c((size_t)(rows + ebk::kMaxGrid) * sizeof(ebk::Partial)); }
+constexpr size_t prefix_bytes(long long rows) { return align256c((size_t)(rows + 1) * sizeof(uint32_t)); }
+constexpr size_t rowunit_bytes(long long rows) { return align256c((size_t)rows * sizeof(int2)); }
+constexpr size_t step_workspace_bytes(long long rows)
+{
+    return partial_bytes(rows) + prefix_bytes(rows) + rowunit_bytes(rows);
+}
 
 struct StepBuffers {
     uint8_t *mask;
@@ -896,12 +918,14 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
 
 // Enqueues the selection kernel over the partial states of this step.
 eb_status launch_select(const eb_params *params, int B, int L, int step, float c, const StepBuffers &sb,
-                        const ebk::Partial *partials, const uint32_t *prefix, long long nvec_row,
+                        const ebk::Partial *partials, const uint32_t *prefix, const int2 *rowunits,
+                        long long nvec_row,
                         int rows, int G, int weighted, int k3_g, cudaStream_t stream)
 {
     ebk::K2Args a2;
     a2.partials = partials;
     a2.prefix = prefix;
+    a2.rowunits = rowunits;
     a2.mask = sb.mask;
     a2.tokens = sb.tokens;
     a2.prev_argmax = sb.prev_argmax;
@@ -927,8 +951,20 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
     a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
     a2.k3_g = k3_g;
-    ebk::k2_select<<<B, ebk::kK2Threads, 0, stream>>>(a2);
-    const cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the selection grid is set up while the row-statistics
+    // grid drains; its griddepcontrol.wait orders the reads of the partial states
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(ebk::kK2Threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ebk::k2_select, a2);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "selection launch: %s", cudaGetErrorString(e));
     return EB_OK;
 }
@@ -957,6 +993,7 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     char *ws = static_cast<char *>(d_ws);
     ebk::Partial *partials = reinterpret_cast<ebk::Partial *>(ws);
     uint32_t *prefix = reinterpret_cast<uint32_t *>(ws + partial_bytes(rows));
+    int2 *rowunits = reinterpret_cast<int2 *>(ws + partial_bytes(rows) + prefix_bytes(rows));
 
     ebk::K1Args a1;
     a1.logits = d_logits;
@@ -964,6 +1001,7 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a1.status = sb.status;
     a1.partials = partials;
     a1.prefix_out = prefix;
+    a1.rowunits = rowunits;
     a1.nvec_row = nvec_row;
     a1.row_bytes = (long long)V * (long long)esize;
     a1.rows = (int)rows;
@@ -976,21 +1014,27 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a1.keys = round_keys(params->seed);
     cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
     g_profile_begin = g_profile_end = nullptr;
-    if (prof_begin && cudaEventRecord(prof_begin, stream) != cudaSuccess)
+    if (prof_begin && record_profile_event(prof_begin, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
-    const size_t smem = ebk::K1Smem::total;
     switch (kind) {
-    case ebk::kF32Vec: ebk::k1_rowstats_tma<ebk::kF32Vec><<<G, ebk::kK1Threads, smem, stream>>>(a1); break;
-    case ebk::kBF16Vec: ebk::k1_rowstats_tma<ebk::kBF16Vec><<<G, ebk::kK1Threads, smem, stream>>>(a1); break;
+    // G counts warps (partition units); whole CTAs of kDirectWarps warps, the tail ones idle
+    case ebk::kF32Vec:
+        ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, 0, stream>>>(a1);
+        break;
+    case ebk::kBF16Vec:
+        ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, 0, stream>>>(a1);
+        break;
     case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
     default: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
-    if (prof_end && cudaEventRecord(prof_end, stream) != cudaSuccess)
+    if (prof_end && record_profile_event(prof_end, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
 
-    return launch_select(params, B, L, step, a1.c, sb, partials, prefix, nvec_row, (int)rows, G,
+    return launch_select(params, B, L, step, a1.c, sb, partials, prefix, rowunits, nvec_row, (int)rows, G,
                          a1.weighted, 0, stream);
 }
 
@@ -1044,7 +1088,7 @@ eb_status launch_unembed(const eb_params *params, int B, int L, int K, int V, co
     a.keys = round_keys(params ? params->seed : 0);
     cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
     g_profile_begin = g_profile_end = nullptr;
-    if (prof_begin && cudaEventRecord(prof_begin, stream) != cudaSuccess)
+    if (prof_begin && record_profile_event(prof_begin, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
     if (logits_out)
         k3::k3_unembed<true><<<G, k3::kThreads, k3::Smem::alloc, stream>>>(th, tw, a);
@@ -1052,10 +1096,10 @@ eb_status launch_unembed(const eb_params *params, int B, int L, int K, int V, co
         k3::k3_unembed<false><<<G, k3::kThreads, k3::Smem::alloc, stream>>>(th, tw, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "unembedding launch: %s", cudaGetErrorString(e));
-    if (prof_end && cudaEventRecord(prof_end, stream) != cudaSuccess)
+    if (prof_end && record_profile_event(prof_end, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
     if (logits_out) return EB_OK;
-    return launch_select(params, B, L, step, a.c, *sb, a.partials, nullptr, 0, (int)M, G, 0, g, stream);
+    return launch_select(params, B, L, step, a.c, *sb, a.partials, nullptr, nullptr, 0, (int)M, G, 0, g, stream);
 }
 
 }  // namespace
@@ -1086,7 +1130,7 @@ size_t eb_workspace_bytes(int B, int L, int V, eb_dtype dtype)
     (void)V;
     (void)dtype;
     if (B < 0 || L < 1) return 0;
-    return partial_bytes((long long)B * L) + prefix_bytes((long long)B * L);
+    return step_workspace_bytes((long long)B * L);
 }
 
 eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype dtype,
@@ -1124,8 +1168,7 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
 namespace {
 
 constexpr long long kNoallocRows = EB_NOALLOC_MAX_ROWS;
-constexpr size_t kNoallocBytes = ((size_t)(kNoallocRows + ebk::kMaxGrid) * sizeof(ebk::Partial) + 255) / 256 * 256 +
-                                 ((size_t)(kNoallocRows + 1) * sizeof(uint32_t) + 255) / 256 * 256;
+constexpr size_t kNoallocBytes = step_workspace_bytes(kNoallocRows);
 
 }  // namespace
 

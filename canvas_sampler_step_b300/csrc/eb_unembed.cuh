@@ -333,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Smem::abort_flag);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the dependent selection grid may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);

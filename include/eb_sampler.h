@@ -131,7 +131,7 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
  *   - a latency-critical loop where the implicit synchronisation of an allocation is not
  *     acceptable.
  * The per-row partial states live instead in one fixed array of device memory inside this
- * library, sized for at most EB_NOALLOC_MAX_ROWS canvas positions (B * L).  That is 557,312
+ * library, sized for at most EB_NOALLOC_MAX_ROWS canvas positions (B * L).  That is 622,848
  * bytes, and every device that loads the library holds them until the process exits.
  *
  * Arguments, results and errors are those of eb_sampler_step, with the workspace supplied by

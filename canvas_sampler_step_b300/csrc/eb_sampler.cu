@@ -227,12 +227,21 @@ constexpr int kDirectThreads = 512;
 constexpr int kDirectWarps = kDirectThreads / 32;
 constexpr int kDirectU = 2;             // vectors per lane per batch (two batches in flight)
 
+// L2 policy for the logits: evicted first, so that streaming them does not push out the
+// workspace (partials, row units) that the selection kernel reads right after.
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+                 : "l"(p), "l"(evict_first_policy()));
     return r;
 }
 
@@ -392,6 +401,8 @@ __device__ __forceinline__ unsigned long long k2_row_start(const K2Args &a, long
                       : (unsigned long long)r * (unsigned long long)a.nvec_row;
 }
 
+constexpr int kMergeBatch = 8;   // partial states fetched per round by the selection kernel
+
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 {
 #pragma unroll
@@ -427,6 +438,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     __shared__ int As[kMaxL];
     __shared__ int Ys[kMaxL];
     __shared__ uint8_t Ms[kMaxL];                // masked before this step
+    __shared__ int Pv[kMaxL];                    // argmax of the previous step
     __shared__ uint8_t Acc[kMaxL];               // accepted at this step
     __shared__ unsigned long long red_sum[kK2Threads / 32];
     __shared__ unsigned long long red_min[kK2Threads / 32];
@@ -446,8 +458,13 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         small_total = 0;
     }
     const long long rowbase = (long long)b * L;
-    // launched as a programmatic dependent of the row-statistics kernel: everything above
-    // reads only what that kernel does not write; wait for its partials here
+    // launched as a programmatic dependent of the row-statistics kernel: the mask and the
+    // previous argmax are not written by it, so they load while it drains; wait for its
+    // partial states here
+    for (int p = tid; p < L; p += blockDim.x) {
+        Ms[p] = a.mask[rowbase + p] ? 1 : 0;
+        Pv[p] = a.prev_argmax[rowbase + p];
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const unsigned long long W = k2_row_start(a, a.rows);
     const unsigned long long G = (unsigned long long)a.G;
@@ -458,28 +475,40 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     int my_unstable = 0, my_bad = 0, my_masked = 0, my_small = 0;
     for (int p = tid; p < L; p += blockDim.x) {
         const long long r = rowbase + p;
-        const unsigned long long w0 = k2_row_start(a, r), w1 = k2_row_start(a, r + 1);
         RowState st = empty_state();
         int flags = 0;
+        // slot list of row r in merge order: [n0, n1) of the fused kernel's (group rank,
+        // column half) pairs, or the row-statistics units u.x .. u.y
+        long long base, stride;
+        int n;
         if (a.k3_g > 0) {
             const long long mb = r >> 7, rl = r & 127;
-            for (int j = 0; j < a.k3_g; ++j) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const Partial q = a.partials[((mb * a.k3_g + j) * 2 + hh) * 128 + rl];
-                    merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
-                    flags |= q.flags;
-                }
-            }
-        } else if (w1 > w0) {
-            // the units that touched row r, recorded by the row-statistics kernel; only when
-            // the total weight is below the unit count can a unit's range be empty
+            base = mb * a.k3_g * 2 * 128 + rl;
+            stride = 128;
+            n = 2 * a.k3_g;
+        } else {
             const int2 u = a.rowunits[r];
-            for (int c = u.x; c <= u.y; ++c) {
-                if (W < G && (unsigned long long)c * W / G >= (unsigned long long)(c + 1) * W / G) continue;
-                const Partial q = a.partials[r + c];
-                merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, a.c);
-                flags |= q.flags;
+            base = r + u.x;
+            stride = 1;
+            n = u.y - u.x + 1;
+        }
+        // loads in batches of kMergeBatch independent requests, merged in slot order
+        for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
+            Partial q[kMergeBatch];
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k)
+                if (i0 + k < n) q[k] = a.partials[base + (long long)(i0 + k) * stride];
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                if (i0 + k >= n) break;
+                // a streaming unit whose weight range is empty wrote nothing (only when the
+                // total weight is below the unit count)
+                if (a.k3_g == 0 && W < G) {
+                    const unsigned long long c = (unsigned long long)(base - r + i0 + k);
+                    if (c * W / G >= (c + 1) * W / G) continue;
+                }
+                merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, a.c);
+                flags |= q[k].flags;
             }
         }
         float H = kLn2 * (log2f(st.S) - st.T2 / st.S);
@@ -488,7 +517,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         if (!isfinite(H) || !isfinite(st.xm) || (flags & kPartialNonfinite)) my_bad |= 1;
         if (flags & kPartialTimeout) my_bad |= 2;
         const bool bad = my_bad != 0;
-        const uint8_t m = a.mask[r] ? 1 : 0;
+        const uint8_t m = Ms[p];
         const int A = st.ai;
         const int Y = m ? st.bi : -1;
         const unsigned long long hq = bad ? 0ull : (unsigned long long)__float2ull_rn(H * 1099511627776.0f);
@@ -496,13 +525,12 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         Hf[p] = H;
         As[p] = A;
         Ys[p] = Y;
-        Ms[p] = m;
         Acc[p] = 0;
         a.entropy[r] = H;
         a.argmax[r] = A;
         a.sampled[r] = Y;
         my_sum += hq;
-        my_unstable |= (a.prev_argmax[r] != A) ? 1 : 0;
+        my_unstable |= (Pv[p] != A) ? 1 : 0;
         if (m) {
             ++my_masked;
             if ((long long)hq <= a.bound_q) {

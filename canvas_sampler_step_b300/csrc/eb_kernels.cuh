@@ -135,8 +135,9 @@ struct K2Args {
     long long bound_q;         // entropy_bound in 2^-40 nats (rounded down)
     long long stop_q;          // stop_entropy * L in 2^-40 nats (rounded up): mean < stop
     int k3_g;                  // > 0: partials come from the fused unembedding kernel, whose
-                               // row block mb, group rank j < k3_g and column half hh write
-                               // slot ((mb k3_g + j) 2 + hh) 128 + row % 128
+                               // row block mb, group rank j < k3_g and column group hh <
+                               // k3_groups write slot ((mb k3_g + j) k3_groups + hh) 128 + row % 128
+    int k3_groups;
 };
 
 // ---------------------------------------------------------------- small device helpers
@@ -394,7 +395,8 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
 // entries against the largest 2^t.  `a` supplies c = log2(e)/T, invT = 1/T, the step and the
 // Philox round keys.  WARP_ROW: the 32 lanes work on the same row (they share the best score
 // when it moves, so every lane must call this with the same trip count; `valid` masks lanes
-// without a group); otherwise every lane owns its row.
+// without a group); otherwise every lane owns its row.  `gumbel` (runtime) switches the
+// sampling part off for a lane whose row is not masked.
 #ifndef EB_PACKED
 #define EB_PACKED 1
 #endif
@@ -404,7 +406,8 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
 template <int N, bool MASKED, bool WARP_ROW, typename Args>
 __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, uint32_t v0, const Args &a,
                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
-                                             PackedSums &q, float &nb, f32x2 &nb2, float &K)
+                                             PackedSums &q, float &nb, f32x2 &nb2, float &K,
+                                             bool gumbel = true)
 {
     float vmax = 0.0f;
     float e[N];
@@ -427,7 +430,7 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                 st.xm = vmax;
                 nb = -vmax * a.c;
                 nb2 = pk2(nb, nb);
-            if (MASKED) K = cand_scale(st.xm, st.best, a.c);
+            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, a.c);
         }
     }
     if (valid) {
@@ -470,7 +473,7 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
     }
     if constexpr (MASKED) {
         bool cand = false;
-        if (valid) {
+        if (valid && gumbel) {
             const uint4 u0 = philox(v0 >> 2, p, (uint32_t)a.step, sw, a.keys);
 #if EB_GROUP_TEST
             float fmin = min3(one_minus_u_plus(u0.x), one_minus_u_plus(u0.y),

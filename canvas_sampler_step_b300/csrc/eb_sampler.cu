@@ -483,9 +483,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         int n;
         if (a.k3_g > 0) {
             const long long mb = r >> 7, rl = r & 127;
-            base = mb * a.k3_g * 2 * 128 + rl;
+            base = mb * a.k3_g * a.k3_groups * 128 + rl;
             stride = 128;
-            n = 2 * a.k3_g;
+            n = a.k3_groups * a.k3_g;
         } else {
             const int2 u = a.rowunits[r];
             base = r + u.x;
@@ -979,6 +979,7 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
     a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
     a2.k3_g = k3_g;
+    a2.k3_groups = ebk::k3::kEpiGroups;
     // programmatic dependent launch: the selection grid is set up while the row-statistics
     // grid drains; its griddepcontrol.wait orders the reads of the partial states
     cudaLaunchConfig_t cfg = {};
@@ -1320,7 +1321,7 @@ size_t eb_unembed_workspace_bytes(int B, int L, int K, int V)
     const long long M = (long long)B * L;
     const long long MB = (M + ebk::k3::BM - 1) / ebk::k3::BM;
     const long long slots = MB > ebk::k3::kMaxCtas ? MB : ebk::k3::kMaxCtas;
-    return align256((size_t)slots * 2 * ebk::k3::BM * sizeof(ebk::Partial));
+    return align256((size_t)slots * ebk::k3::kEpiGroups * ebk::k3::BM * sizeof(ebk::Partial));
 }
 
 namespace {

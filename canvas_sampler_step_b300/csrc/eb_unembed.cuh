@@ -8,24 +8,27 @@
 // streamed logits.  (DiffusionGemma model card, "Best practices" section 1: the sampler consumes
 // the decoder's full-vocabulary logits of every canvas position at every denoising step.)
 //
-// One CTA per SM, 320 threads, warp-specialised:
+// One CTA per SM, 576 threads, warp-specialised:
 //   warp 0      TMA producer: per 64-wide K slice one 128 x 64 box of h (K-major, 128-byte
 //               swizzle) and four 64 x 64 boxes of W (V contiguous, i.e. an N-major B operand)
 //               into a 4-stage shared-memory ring, completion counted on mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
 //               tcgen05.mma (M=128, N=256, K=16, kind::f16, bf16 x bf16 -> fp32) from one lane;
 //               tcgen05.commit releases ring stages and hands finished accumulators over;
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (one canvas row per thread)
-//               and accumulator columns 128 ((w - 2) / 4) .. +127 with tcgen05.ld, 32 columns at
-//               a time, and updates its row's state; it frees the accumulator for the next tile.
+//   warps 2..17 epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (one canvas row per thread)
+//               and accumulator columns 64 ((w - 2) / 4) .. +63 with tcgen05.ld, 32 columns at
+//               a time (the next load in flight while a chunk is consumed), and updates its row's
+//               state in groups of 8 columns with the streaming kernel's per-group body; it frees
+//               the accumulator for the next tile.
 // The two accumulators let the MMA of tile i+1 run while the epilogue consumes tile i.
 //
 // Schedule: the M x V output is cut into MB = ceil(M/128) row blocks and NB = ceil(V/256)
 // column tiles.  With MB <= G (CTAs), CTA c owns row block c % MB and column tiles j, j+g, ...
 // (j = c / MB, g = G / MB), so the MB CTAs that share j read the same W tile at about the same
 // time (one HBM read, the rest from L2) and each CTA keeps its rows' state in registers for its
-// whole column range.  Partial state of (row block mb, group rank j, column half hh, row lane)
-// lands in slot ((mb g + j) 2 + hh) 128 + lane; the selection kernel merges them in that order.
+// whole column range.  Partial state of (row block mb, group rank j, column group hh, row
+// lane) lands in slot ((mb g + j) kEpiGroups + hh) 128 + lane; the selection kernel merges them
+// in that order.
 //
 // Every mbarrier wait is bounded.  A role whose wait gives up raises a shared abort flag, the
 // others leave their loops at their next wait, the producer waits (bounded) for its copies in
@@ -52,7 +55,13 @@ constexpr int kABytes = BM * BK * 2;          // 16 KiB
 constexpr int kBBoxBytes = 64 * BK * 2;       // 8 KiB: 64 columns x 64 K rows
 constexpr int kBBytes = BN * BK * 2;          // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kEpiWarps = 8;
+#ifndef EB_EPI_WARPS
+#define EB_EPI_WARPS 16
+#endif
+constexpr int kEpiWarps = EB_EPI_WARPS;             // 8 or 16
+constexpr int kEpiGroups = kEpiWarps / 4;           // column groups (each covers all 128 lanes)
+constexpr int kEpiCols = BN / kEpiGroups;           // accumulator columns per epilogue warp
+static_assert(kEpiCols % 64 == 0, "each epilogue warp takes whole pairs of 32-column chunks");
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kMaxCtas = 1024;
@@ -151,10 +160,10 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
                  : "memory");
 }
 
-// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&x)[32])
+// Issues the load of 32 consecutive fp32 accumulator columns of this thread's TMEM lane; the
+// registers hold the values only after tc_wait32 on the same array.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
-    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -165,9 +174,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&x)[32])
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+}
+
+// Waits for every outstanding tcgen05.ld of the thread.  The array is an in/out operand so
+// that no use of the loaded registers moves above the wait.
+__device__ __forceinline__ void tc_wait32(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 // Bounded wait that also gives up as soon as another role raised the abort flag.
@@ -225,92 +245,36 @@ struct Tiles {
 
 // ------------------------------------------------------------------ epilogue math
 
-// One chunk of 32 accumulator columns (raw logits x, first column v0) of a row, nv of them
-// valid (< V).  Same arithmetic as the streaming kernel's per-vector body.
-template <bool TAIL>
-__device__ __forceinline__ void epi_chunk(const float (&x)[32], int nv, int v0, bool masked,
-                                          uint32_t p, uint32_t sw, const Args &a, RowState &st,
-                                          float &nb, float &K)
+// The 32 accumulator columns r (entries v0 .., v0 a multiple of 32) of this thread's row, as
+// four groups of 8 through the streaming kernel's per-group body (each lane owns its row;
+// `gumbel` is off for lanes whose row is not masked).
+__device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], int v0, bool on, bool gumbel, const Args &a,
+                                          uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                          float &nb, f32x2 &nb2, float &K)
 {
-    float vmax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-        const float m2 = TAIL ? fmaxf(j < nv ? x[j] : -INFINITY, j + 1 < nv ? x[j + 1] : -INFINITY)
-                              : fmaxf(x[j], x[j + 1]);
-        vmax = fmaxf(vmax, m2);
-    }
-    if (vmax > st.xm) {
-        const float d = (st.xm - vmax) * a.c;
-        const float sc = ex2(d);
-        st.T2 = sc == 0.0f ? 0.0f : sc * fmaf(d, st.S, st.T2);
-        st.S = sc == 0.0f ? 0.0f : st.S * sc;
-        int j0 = 31;
+    for (int g = 0; g < 4; ++g) {
+        float x[8];
 #pragma unroll
-        for (int j = 31; j >= 0; --j)
-            if (x[j] == vmax && (!TAIL || j < nv)) j0 = j;
-        st.ai = v0 + j0;
-        st.xm = vmax;
-        nb = -vmax * a.c;
-        if (masked) K = cand_scale(st.xm, st.best, a.c);
-    }
-    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, t4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    bool any = false;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float e[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = 4 * q + i;
-            const float t = fmaf(x[j], a.c, nb);
-            e[i] = ex2(t);
-            if (!TAIL || j < nv) {
-                s4[i] += e[i];
-                t4[i] = fmaf(t, e[i], t4[i]);
-            }
-        }
-        if (masked) {
-            const uint4 w = philox((uint32_t)((v0 >> 2) + q), p, (uint32_t)a.step, sw, a.keys);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool ok = !TAIL || (4 * q + i) < nv;
-                any |= ok && (one_minus_u_plus(ww[i]) < fmaf(e[i], K, kCandAdd));
-            }
-        }
-    }
-    st.S += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    st.T2 += (t4[0] + t4[1]) + (t4[2] + t4[3]);
-    if (any) {
-        // rare: recompute the chunk's words and take the exact score of every candidate
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint4 w = philox((uint32_t)((v0 >> 2) + q), p, (uint32_t)a.step, sw, a.keys);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 4 * q + i;
-                if (TAIL && j >= nv) continue;
-                const float e = ex2(fmaf(x[j], a.c, nb));
-                const float f = one_minus_u_plus(ww[i]);
-                if (f < fmaf(e, K, kCandAdd)) {
-                    const float delta = f - kOneMinusHalfUlp;      // 1 - u, exact
-                    const float E = -log1pf(-delta);               // -ln u
-                    const float score = x[j] * a.invT - logf(E);
-                    const int idx = v0 + j;
-                    if (better(score, idx, st.best, st.bi)) {
-                        st.best = score;
-                        st.bi = idx;
-                    }
-                }
-            }
-        }
-        K = cand_scale(st.xm, st.best, a.c);
+        for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[8 * g + j]);
+        const int vg = v0 + 8 * g;
+        consume_vals<8, true, false>(x, on && vg < a.V, (uint32_t)vg, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
     }
 }
 
 __device__ __forceinline__ int partial_flags(const RowState &st, bool ok)
 {
     return (ok ? 0 : kPartialTimeout) | ((isnan(st.S) || isnan(st.T2)) ? kPartialNonfinite : 0);
+}
+
+// Plain-product mode: the 32 accumulator columns of row r written out as fp32 logits.
+__device__ __forceinline__ void store_logits(const uint32_t (&x)[32], int r, int v0, const Args &a)
+{
+    if (r >= a.M) return;
+    float *o = a.logits + (long long)r * a.V + v0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (v0 + j < a.V) o[j] = __uint_as_float(x[j]);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -432,21 +396,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                    // TMEM lane quarter of this warp
-        const int hh = (warp - 2) >> 2;            // accumulator column half
+        const int hh = (warp - 2) >> 2;            // accumulator column group
         const int rl = 32 * q + lane;              // row within the block
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(hh * (BN / 2));
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(hh * kEpiCols);
         uint32_t ti = 0;
         bool ok = true;
         int cur_mb = -1;
         RowState st = empty_state();
+        PackedSums qs;
+        packed_zero(qs);
         float nb = 0.0f, K = 0.0f;
+        f32x2 nb2 = 0ull;
+        const f32x2 c2 = pk2(a.c, a.c);
         bool row_on = false, masked = false;
         uint32_t p = 0, sw = 0;
         for (; tl.valid();) {
             if (tl.mb != cur_mb) {
-                if (!LOGITS && cur_mb >= 0 && row_on)
-                    write_partial(&a.partials[((long long)(cur_mb * a.g + tl.j) * 2 + hh) * BM + rl], st,
+                if (!LOGITS && cur_mb >= 0 && row_on) {
+                    packed_fold(qs, st);
+                    write_partial(&a.partials[((long long)(cur_mb * a.g + tl.j) * kEpiGroups + hh) * BM + rl], st,
                                   partial_flags(st, ok));
+                }
                 cur_mb = tl.mb;
                 const int r = cur_mb * BM + rl;
                 row_on = r < a.M;
@@ -458,7 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sw = (kStreamGumbel << 24) | (uint32_t)b;
                 }
                 st = empty_state();
+                packed_zero(qs);
                 nb = -st.xm * a.c;
+                nb2 = pk2(nb, nb);
                 K = cand_scale(st.xm, st.best, a.c);
             }
             const uint32_t acc = ti & 1u, use = ti >> 1;
@@ -468,25 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
             tc_fence_after();
             if (ok) {
-                const int vbase = tl.n * BN + hh * (BN / 2);
+                const int vbase = tl.n * BN + hh * kEpiCols;
+                const uint32_t base = lane_addr + acc * BN;
+                // two register buffers: the load of the next chunk is in flight while one runs
+                uint32_t ra[32], rb[32];
+                tc_ld32(base, ra);
+                tc_wait32(ra);
 #pragma unroll 1
-                for (int ch = 0; ch < BN / 2 / 32; ++ch) {
-                    float x[32];
-                    tc_ld32(lane_addr + acc * BN + (uint32_t)(32 * ch), x);
+                for (int ch = 0; ch < kEpiCols / 32; ch += 2) {
+                    tc_ld32(base + (uint32_t)(32 * (ch + 1)), rb);
                     const int v0 = vbase + 32 * ch;
-                    const int nv = min(32, a.V - v0);
-                    if (LOGITS) {
-                        const int r = cur_mb * BM + rl;
-                        if (r < a.M) {
-                            float *o = a.logits + (long long)r * a.V + v0;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (j < nv) o[j] = x[j];
-                        }
-                    } else if (row_on && nv > 0) {
-                        if (nv >= 32) epi_chunk<false>(x, nv, v0, masked, p, sw, a, st, nb, K);
-                        else epi_chunk<true>(x, nv, v0, masked, p, sw, a, st, nb, K);
-                    }
+                    if (LOGITS) store_logits(ra, cur_mb * BM + rl, v0, a);
+                    else epi_chunk(ra, v0, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K);
+                    tc_wait32(rb);
+                    if (ch + 2 < kEpiCols / 32) tc_ld32(base + (uint32_t)(32 * (ch + 2)), ra);
+                    if (LOGITS) store_logits(rb, cur_mb * BM + rl, v0 + 32, a);
+                    else epi_chunk(rb, v0 + 32, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K);
+                    if (ch + 2 < kEpiCols / 32) tc_wait32(ra);
                 }
             }
             tc_fence_before();
@@ -495,9 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ti;
             tl.advance();
         }
-        if (!LOGITS && cur_mb >= 0 && row_on)
-            write_partial(&a.partials[((long long)(cur_mb * a.g + tl.j) * 2 + hh) * BM + rl], st,
+        if (!LOGITS && cur_mb >= 0 && row_on) {
+            packed_fold(qs, st);
+            write_partial(&a.partials[((long long)(cur_mb * a.g + tl.j) * kEpiGroups + hh) * BM + rl], st,
                           partial_flags(st, ok));
+        }
     }
     tc_fence_before();
     __syncthreads();

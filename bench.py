@@ -39,7 +39,17 @@ TEMPERATURE = 0.8
 WORKLOAD = ("single EB sampler step: B=1 canvas, L=256 positions, V=262144 bf16 logits "
             "(2.5*N(0,1) + U(0,12) peak per position), 128 of 256 masked, T=0.8")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k1_rowstats_bf16_single_step.md")
-KERNEL_SRC = os.path.join(ROOT, "canvas_sampler_step_b300", "csrc", "eb_sampler.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "canvas_sampler_step_b300", "csrc", f)
+               for f in ("eb_sampler.cu", "eb_kernels.cuh")]
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the row-statistics kernel's sources."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def parse_args(argv=None):
@@ -50,6 +60,10 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("single", "fused", "loop"), default="single",
+                    help="single: the single-step workload (default, the headline line); fused: "
+                         "the fused unembedding + sampler step (4 x 256 positions, K=2048); loop: "
+                         "the adaptive 48-step loop over 8 canvases with the stand-in denoiser")
     return ap.parse_args(argv)
 
 
@@ -111,7 +125,7 @@ def recorded_traffic():
     or None when absent or taken on a different kernel source."""
     try:
         text = open(TRAFFIC_FILE).read()
-        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        src_hash = kernel_source_hash()
     except OSError:
         return None
     vals = {}
@@ -536,11 +550,244 @@ def run_reference(args, rank, world, local):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------------ fused unembedding workload
+
+FUSED_METRIC = ("EB-sampler fused unembedding steps/s at 4x256 positions, K=2048, V=262144 bf16; "
+                "achieved tensor TFLOP/s vs B300 peak")
+FB, FL, FK, FV = 4, 256, 2048, 262144
+FUSED_FLOP = 2 * FB * FL * FK * FV
+
+
+def measured_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1400.0, 1800.0, "fallback"
+
+
+def run_fused(args, rank, world, local):
+    """One step = eb_unembed_sample over 1024 fresh all-masked positions: h [1024, 2048] x
+    W [2048, 262144] on the tensor cores, the row statistics in the epilogue, the selection.
+    h and W are resident (W is the model's unembedding matrix); each graph replay restores
+    the canvas states first."""
+    import ctypes
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth.device as synth_dev
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    lib = eb.lib()
+    synth_dev.lib()
+    stream = torch.cuda.current_stream(device)
+    h = torch.empty((FB * FL, FK), dtype=torch.int16, device=device)
+    W = torch.empty((FK, FV), dtype=torch.int16, device=device)
+    synth_dev.unembed_inputs(0, FB * FL, FK, FV, 0.02, 0.05, h, W)
+    K, Wm = args.steps, args.warmup
+    N = max(d for d in range(1, min(K, 20) + 1) if K % d == 0)
+    R = K // N
+    canv = [eb.Canvas(FB, FL, FV, eb.EB_BF16, device=device) for _ in range(N)]
+    pristine = {k: getattr(canv[0], k).clone() for k in ("mask", "tokens", "prev_argmax", "status",
+                                                          "steps_taken")}
+    ws_bytes = eb.eb_unembed_workspace_bytes(FB, FL, FK, FV)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    params = eb.eb_default_params(seed=0)
+
+    def one(c, sp):
+        eb.eb_unembed_sample(params, FB, FL, FK, FV, h, W, 0, 0.8, c.mask, c.tokens, c.prev_argmax,
+                             c.status, c.steps_taken, c.entropy, c.argmax, c.sampled, c.selected,
+                             c.committed, c.mean_entropy, ws, ws_bytes, sp)
+
+    warm = eb.Canvas(FB, FL, FV, eb.EB_BF16, device=device)
+    for _ in range(max(Wm, 3)):
+        for k, v in pristine.items():
+            getattr(warm, k).copy_(v)
+        one(warm, stream.cuda_stream)
+    torch.cuda.synchronize()
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(N)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(N)]
+    for e in kb + ke:
+        e.record(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        graph.capture_begin()
+        csp = torch.cuda.current_stream(device).cuda_stream
+        for j in range(N):
+            for k, v in pristine.items():
+                getattr(canv[j], k).copy_(v)
+            lib.eb_set_profile_events(kb[j].cuda_event, ke[j].cuda_event)
+            one(canv[j], csp)
+        graph.capture_end()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(dist, local)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(R):
+            graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, local)
+    elapsed = start.elapsed_time(end) / 1e3
+    k3_ms = [b.elapsed_time(e) for b, e in zip(kb, ke)]
+    value, slowest = aggregate(K, elapsed, world, dist, local)
+    for c in canv:
+        if not ((c.status == 0).all() and (c.committed >= 1).all()):
+            raise RuntimeError("timed steps did not run the expected workload")
+    sustained, burst, kind = measured_tensor_peak()
+    k3_s = statistics.mean(k3_ms) / 1e3
+    achieved = FUSED_FLOP / k3_s / 1e12
+
+    # end to end: per step the hidden states and canvas state go host -> device, the step
+    # runs, the results come back (W stays resident: it is the model's weight)
+    n_e2e = max(1, min(args.e2e_steps, 50))
+    h_host = h.cpu().pin_memory()
+    in_keys = ("mask", "tokens", "prev_argmax", "status")
+    hstate = {k: pristine[k].cpu().pin_memory() for k in in_keys}
+    out_keys = ("tokens", "mask", "status", "entropy", "argmax", "sampled", "selected")
+    c = canv[0]
+    hout = {k: torch.empty_like(getattr(c, k), device="cpu").pin_memory() for k in out_keys}
+    h_dev = torch.empty_like(h)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        h_dev.copy_(h_host, non_blocking=True)
+        for k in in_keys:
+            getattr(c, k).copy_(hstate[k], non_blocking=True)
+        eb.eb_unembed_sample(params, FB, FL, FK, FV, h_dev, W, 0, 0.8, c.mask, c.tokens,
+                             c.prev_argmax, c.status, c.steps_taken, c.entropy, c.argmax,
+                             c.sampled, c.selected, c.committed, c.mean_entropy, ws, ws_bytes,
+                             stream.cuda_stream)
+        for k in out_keys:
+            hout[k].copy_(getattr(c, k), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(n_e2e, e0.elapsed_time(e1) / 1e3, world, dist, local)
+    h2d = h_host.numel() * 2 + sum(v.numel() * v.element_size() for v in hstate.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    out = {
+        "metric": FUSED_METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": slowest * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox / Box-Muller h and W, eb_synth)",
+        "config": {"workload": "fused unembedding + EB sampler step: h [1024, 2048] ~ N(0,1) x W "
+                               "[2048, 262144] ~ N(0, 0.02^2) + 0.05 planted per row, bf16, "
+                               "4 canvases x 256 positions all masked, T=0.8",
+                   "B": FB, "L": FL, "K": FK, "V": FV,
+                   "l2": "W (1 GiB) > 126 MB L2, read once per step",
+                   "launch": f"CUDA graph of {N} steps (+ canvas-state restores) replayed {R} times",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "k3_unembed", "achieved": achieved,
+                     "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
+                     "peak_kind": f"{kind} bf16 sustained (burst {burst})", "traffic": None,
+                     "k3_ms_mean": statistics.mean(k3_ms), "flop_per_launch": FUSED_FLOP},
+        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": n_e2e, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ adaptive loop workload
+
+LOOP_METRIC = ("EB adaptive denoising loop: canvas-steps/s over 8 canvases x 256 x 262144 bf16 "
+               "(peak growth 0.1-0.8), stand-in denoiser included")
+
+
+def run_loop(args, rank, world, local):
+    """The whole <= 48-step loop (eb_sample_canvas) over 8 canvases whose logits the seeded
+    stand-in denoiser regenerates on the device every step; reports steps to stop per canvas
+    and positions committed per step.  One 'step' of the metric is one canvas-step."""
+    import ctypes
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth
+    import eb_synth.device as synth_dev
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    eb.lib()
+    synth_dev.lib()
+    stream = torch.cuda.current_stream(device)
+    cfg = eb_synth.cfg3()
+    recipe = synth_dev.Recipe.of(cfg)
+    buf = torch.empty((cfg.B, cfg.L, cfg.V), dtype=torch.int16, device=device)
+    params = eb.eb_default_params(seed=0)
+    runs = max(1, args.steps // 200)
+
+    def loop():
+        c = eb.Canvas(cfg.B, cfg.L, cfg.V, eb.EB_BF16, device=device)
+        ran = c.run(params, synth_dev.callback_address(), ctypes.addressof(recipe), buf, poll_every=4)
+        return c, ran
+
+    for _ in range(max(1, args.warmup // 100)):
+        loop()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    canvas_steps = 0
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(runs):
+            c, ran = loop()
+            canvas_steps += int(c.steps_taken.sum().item())
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, local)
+    elapsed = start.elapsed_time(end) / 1e3
+    value, slowest = aggregate(canvas_steps, elapsed, world, dist, local)
+    st = c.steps_taken.cpu().numpy().tolist()
+    com = c.committed_per_step.cpu().numpy()
+    out = {
+        "metric": LOOP_METRIC, "value": value, "unit": "canvas-steps/s", "n_gpus": world,
+        "steps": canvas_steps, "warmup": args.warmup, "ms_per_step": slowest * 1e3 / canvas_steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Philox / Box-Muller stand-in denoiser, eb_synth)",
+        "config": {"workload": "adaptive loop: 8 canvases x 256 positions x 262144 bf16, sigma 3, "
+                               "peak U(0,4) + r s, r in (0.1, 0.2, 0.4, 0.8), up to 48 steps, "
+                               "logits regenerated on the device every step",
+                   "loops": runs, "parallelism": f"replicas x{world}"},
+        "steps_to_stop": st,
+        "stop_reason": c.status.cpu().numpy().tolist(),
+        "committed_per_step_mean": float(com[com > 0].mean()) if (com > 0).any() else 0.0,
+        "gpu_launches": None,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
+    elif args.workload == "fused":
+        run_fused(args, rank, world, local)
+    elif args.workload == "loop":
+        run_loop(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 

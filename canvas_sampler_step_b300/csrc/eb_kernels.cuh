@@ -519,7 +519,8 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
 template <int VEC, bool MASKED>
 __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32_t jvec, const K1Args &a,
                                                uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
-                                               PackedSums &q, float &nb, f32x2 &nb2, float &K)
+                                               PackedSums &q, float &nb, f32x2 &nb2, float &K,
+                                               bool gumbel = true)
 {
     float x[VEC];
     if constexpr (VEC == 8) {
@@ -535,7 +536,7 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
         x[2] = __uint_as_float(r.z);
         x[3] = __uint_as_float(r.w);
     }
-    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, p, sw, c2, st, q, nb, nb2, K);
+    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
 }
 
 // ---------------------------------------------------------------- mbarrier / bulk copy PTX

@@ -252,23 +252,26 @@ __device__ __forceinline__ void load_full(uint4 (&r)[U], const uint4 *src, uint3
     for (int u = 0; u < U; ++u) r[u] = ld_stream(src + jb + lane + 32u * (uint32_t)u);
 }
 
-template <int VEC, bool MASKED, int U>
+template <int VEC, int U>
 __device__ __forceinline__ void consume_full(const uint4 (&r)[U], uint32_t jb, uint32_t lane, const K1Args &a,
                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
-                                             float &nb, f32x2 &nb2, float &K)
+                                             float &nb, f32x2 &nb2, float &K, bool gumbel)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        consume_packed<VEC, MASKED>(r[u], true, jb + lane + 32u * (uint32_t)u, a, p, sw, c2, st, q, nb, nb2, K);
+        consume_packed<VEC, true>(r[u], true, jb + lane + 32u * (uint32_t)u, a, p, sw, c2, st, q, nb, nb2, K,
+                                  gumbel);
 }
 
 // One row segment [j0, j1) of a warp: whole batches of 32 U vectors run without bounds
 // checks from two register buffers (the next batch loads while the current one is consumed),
 // the remainder with checks.
-template <int VEC, bool MASKED, int U>
+// One code instance serves masked and unmasked rows (`gumbel` is warp-uniform), which keeps
+// the unrolled loop small enough for the instruction cache.
+template <int VEC, int U>
 __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
                                                uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
-                                               PackedSums &q)
+                                               PackedSums &q, bool gumbel)
 {
     constexpr uint32_t kBatch = 32u * U;
     const uint32_t lane = threadIdx.x & 31;
@@ -282,11 +285,11 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
         for (uint32_t jb = j0;; jb += 2 * kBatch) {
             const bool hasB = jb + kBatch < jf;
             if (hasB) load_full<U>(B, src, jb + kBatch, lane);
-            consume_full<VEC, MASKED, U>(A, jb, lane, a, p, sw, c2, st, q, nb, nb2, K);
+            consume_full<VEC, U>(A, jb, lane, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
             if (!hasB) break;
             const bool hasA = jb + 2 * kBatch < jf;
             if (hasA) load_full<U>(A, src, jb + 2 * kBatch, lane);
-            consume_full<VEC, MASKED, U>(B, jb + kBatch, lane, a, p, sw, c2, st, q, nb, nb2, K);
+            consume_full<VEC, U>(B, jb + kBatch, lane, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
             if (!hasA) break;
         }
     }
@@ -295,7 +298,7 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
         const uint32_t idx = jb + lane;
         const bool valid = idx < j1;
         const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-        consume_packed<VEC, MASKED>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K);
+        consume_packed<VEC, true>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
     }
 }
 
@@ -332,8 +335,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
         RowState st = empty_state();
         PackedSums q;
         packed_zero(q);
-        if (masked) direct_segment<VEC, true, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q);
-        else direct_segment<VEC, false, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q);
+        direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked);
         packed_fold(q, st);
         const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
         warp_merge(st, a.c);

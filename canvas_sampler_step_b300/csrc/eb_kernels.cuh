@@ -418,7 +418,33 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
     // a new running maximum is rare after the first groups; the vote keeps this a real branch
     // (the compiler would otherwise predicate the whole block into every group)
     const bool newmax = valid && vmax > st.xm;
-    if (__any_sync(WARP_ROW ? 0xFFFFFFFFu : __activemask(), newmax)) {
+    if constexpr (WARP_ROW) {
+        // the lanes share one running maximum (the reference of every lane's sums), so a new
+        // maximum is a record of the whole warp's part of the row, not of each lane's
+        if (__any_sync(0xFFFFFFFFu, newmax)) {
+            float wm = valid ? vmax : -INFINITY;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+            // first entry holding it: entries grow with the lane within one group of vectors
+            int idx = 0x7FFFFFFF;
+            if (valid && vmax == wm) {
+                int j0 = N - 1;
+#pragma unroll
+                for (int j = N - 1; j >= 0; --j)
+                    if (x[j] == wm) j0 = j;
+                idx = (int)(v0 + (uint32_t)j0);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
+            const float d = (st.xm - wm) * a.c;
+            packed_rescale(q, d, ex2(d));
+            st.ai = idx;
+            st.xm = wm;
+            nb = -wm * a.c;
+            nb2 = pk2(nb, nb);
+            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, a.c);
+        }
+    } else if (__any_sync(__activemask(), newmax)) {
         if (newmax) {
                 const float d = (st.xm - vmax) * a.c;
                 packed_rescale(q, d, ex2(d));

@@ -190,6 +190,49 @@ def test_loop_parity_mixed_batch_small():
     assert rep.canvases > 50
 
 
+def test_loop_adaptive_stop_parity():
+    """Dominant, fixed peaks: the entropy is ~0 everywhere and the argmax never moves, so every
+    canvas stops adaptively at step 1 and its still-masked positions take the argmax.  Which
+    position step 0 commits is an order tie (all entropies ~0), but every committed token is
+    the peak either way: stop reason, stop step and final tokens match the oracle's."""
+    cfg = eb_synth.Peaked(3, 128, 4096, "f32", 1.0, 40.0, 0.0, (0.0, 0.0, 0.0), (21, 22, 23))
+    gp, op = params_pair(seed=21, entropy_bound=-1.0)
+    rep, hist, c = _lockstep(cfg, params_kw={"entropy_bound": -1.0})
+    final = hist[-1]
+    assert (final["status"] == eb.EB_STOP_ADAPTIVE).all()
+    assert (final["steps_taken"] == 2).all()
+    assert final["mask"].sum() == 0
+    # step 0 committed one position per canvas, step 1 the remaining 127
+    assert hist[0]["committed"].tolist() == [1, 1, 1]
+    assert hist[1]["committed"].tolist() == [127, 127, 127]
+    ost = oracle.run_loop(lambda s, st: cfg.logits(s), 3, 128, op)
+    assert ost.status.tolist() == [oracle.ADAPTIVE] * 3 and ost.steps_taken.tolist() == [2, 2, 2]
+    assert np.array_equal(final["tokens"], ost.tokens)
+
+
+def test_loop_cap_and_complete_parity():
+    """Noisy logits that never settle: with the bound at -1 exactly one position commits per
+    step, so a 5-step run ends at the cap with the rest filled by the argmax, while a canvas of
+    4 positions completes at step 3; both match the oracle."""
+    cfg = eb_synth.Peaked(1, 16, 512, "f32", 3.0, 0.0, 0.0, (0.0,), (31,))
+    rep, hist, c = _lockstep(cfg, params_kw={"entropy_bound": -1.0, "max_steps": 5})
+    assert hist[-1]["status"][0] == eb.EB_STOP_CAP and hist[-1]["steps_taken"][0] == 5
+    assert hist[-1]["committed"][0] == 16 - 4
+    cfg2 = eb_synth.Peaked(1, 4, 512, "f32", 3.0, 0.0, 0.0, (0.0,), (32,))
+    rep2, hist2, c2 = _lockstep(cfg2, params_kw={"entropy_bound": -1.0})
+    assert hist2[-1]["status"][0] == eb.EB_STOP_COMPLETE and hist2[-1]["steps_taken"][0] == 4
+
+
+def test_step_parity_longest_canvas():
+    """L = 1024 positions (the largest canvas the selection kernel takes) with many
+    low-entropy positions: the general (shared-memory) sort path."""
+    cfg = eb_synth.Peaked(1, 1024, 256, "f32", 1.0, 25.0, 10.0, (0.0,), (41,))
+    g, res, ost, running = _run_step(cfg, 0)
+    rep = Report()
+    compare_step(g, res, ost, running, rep)
+    assert res.committed[0] > 32
+
+
 def _check_selection_properties(g, mask_before, bound=np.float32(0.1)):
     """Selection validity from the GPU's own entropies: the committed masked positions
     are the k lowest (H, p) and k follows the prefix rule (up to the tie window)."""

@@ -12,11 +12,13 @@
 //     instructions per byte, and halted canvases cost nothing.  Warp g writes one partial
 //     state for every row its range touches to slot (row + g) of the workspace (the (row,
 //     warp) pairs form a staircase, so row + g is unique).
-//   * Data movement.  Each warp streams its row segments with coalesced 16-byte loads that
-//     bypass L1 (ld.global.nc.L1::no_allocate), two vectors per lane per batch, the next batch
-//     in flight while the current one is consumed; whole batches run without bounds checks.
-//     (A TMA bulk-copy ring with a producer warp measured slower on this workload: 81.7 us
-//     against 71-79 us, its consumers idling on the ring's barriers.)
+//   * Data movement.  Each lane copies the 16-byte vectors it will consume, two per batch, with
+//     cp.async (L2 evict-first, no L1) into its own shared-memory slots four batches ahead of
+//     use, and waits only for its own oldest group; warps read their slots conflict-free and
+//     run whole batches without bounds checks.  (A TMA bulk-copy ring with a producer warp
+//     measured slower on this workload: 81.7 us against 78 us, its consumers idling on the
+//     ring's barriers; register double buffering had too little in flight: 47.6 us against
+//     41.9 us on unmasked rows.)
 //   * Per element: t = x * log2(e)/T - xm * log2(e)/T, e = 2^t (MUFU), S += e, T2 += t e,
 //     with xm the running maximum of the thread's raw logits (first index kept for the
 //     argmax); the FMAs and adds run on packed f32x2 pairs.  H = ln 2 (log2 S - T2 / S)
@@ -48,8 +50,8 @@ constexpr int kMaxWeightedRows = 4096;
 constexpr int kK2Threads = 256;
 constexpr int kMaxL = 1024;
 constexpr int kMaxGrid = 8192;
-constexpr int kWeightUnmasked = 6;                 // relative cost of a vector of an unmasked row
-constexpr int kWeightMasked = 13;                  // ... and of a masked row (measured 2.16 : 1)
+constexpr int kWeightUnmasked = 11;                // relative cost of a vector of an unmasked row
+constexpr int kWeightMasked = 26;                  // ... and of a masked row (measured 2.36 : 1)
 constexpr uint32_t kWaitLimit = 1u << 26;           // mbarrier polls before giving up
 
 constexpr float kLog2e = 1.4426950408889634f;

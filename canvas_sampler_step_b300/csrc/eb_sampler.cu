@@ -225,7 +225,7 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, R
 // after the prefix is built.
 constexpr int kDirectThreads = 512;
 constexpr int kDirectWarps = kDirectThreads / 32;
-constexpr int kDirectU = 2;             // vectors per lane per batch (two batches in flight)
+constexpr int kDirectU = 2;             // vectors per lane per batch
 
 // L2 policy for the logits: evicted first, so that streaming them does not push out the
 // workspace (partials, row units) that the selection kernel reads right after.
@@ -302,6 +302,72 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
     }
 }
 
+// --- the same segment with a deeper prefetch: each lane copies the vectors it will consume
+// with cp.async (16 bytes each, L2 evict-first, no L1) into its own shared-memory slots,
+// kAsyncDepth batches ahead, and waits only for its own oldest group (no cross-lane barrier).
+#ifndef EB_ASYNC_DEPTH
+#define EB_ASYNC_DEPTH 4
+#endif
+constexpr int kAsyncDepth = EB_ASYNC_DEPTH;
+constexpr int kDirectStageBytes = kAsyncDepth * kDirectU * kDirectThreads * 16;
+
+__device__ __forceinline__ void cp_async16(uint4 *dst, const uint4 *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int VEC, int U>
+__device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
+                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                              bool gumbel, uint4 *stage)
+{
+    constexpr uint32_t kBatch = 32u * U;
+    const uint32_t tid = threadIdx.x, lane = tid & 31;
+    float nb = -st.xm * a.c;
+    f32x2 nb2 = pk2(nb, nb);
+    float K = cand_scale(st.xm, st.best, a.c);
+    const uint32_t nfull = (j1 - j0) / kBatch;
+    const uint32_t jf = j0 + nfull * kBatch;
+    const uint64_t pol = evict_first_policy();
+    // stage layout [depth][U][thread]: consecutive lanes read consecutive 16-byte slots
+    auto slot = [&](uint32_t b, int u) { return stage + ((b % kAsyncDepth) * U + u) * kDirectThreads + tid; };
+#pragma unroll
+    for (int k = 0; k < kAsyncDepth - 1; ++k) {
+        if ((uint32_t)k < nfull)
+#pragma unroll
+            for (int u = 0; u < U; ++u) cp_async16(slot(k, u), src + j0 + k * kBatch + lane + 32u * u, pol);
+        cp_async_commit();
+    }
+    for (uint32_t b = 0; b < nfull; ++b) {
+        const uint32_t bn = b + kAsyncDepth - 1;
+        if (bn < nfull)
+#pragma unroll
+            for (int u = 0; u < U; ++u) cp_async16(slot(bn, u), src + j0 + bn * kBatch + lane + 32u * u, pol);
+        cp_async_commit();
+        cp_async_wait<kAsyncDepth - 1>();
+        const uint32_t jb = j0 + b * kBatch;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            consume_packed<VEC, true>(*slot(b, u), true, jb + lane + 32u * u, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+    }
+    cp_async_wait<0>();
+#pragma unroll 1
+    for (uint32_t jb = jf; jb < j1; jb += 32u) {
+        const uint32_t idx = jb + lane;
+        const bool valid = idx < j1;
+        const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+        consume_packed<VEC, true>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+    }
+}
+
 template <int KIND, int U>
 __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1Args a)
 {
@@ -310,6 +376,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
     __shared__ uint32_t P[kMaxWeightedRows + 1];
     __shared__ uint8_t mflag[kMaxWeightedRows];
     __shared__ uint32_t scan[32];
+    extern __shared__ __align__(16) uint4 stage[];   // kAsyncDepth x U x kDirectThreads vectors
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the dependent selection grid may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;");
@@ -335,7 +402,8 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
         RowState st = empty_state();
         PackedSums q;
         packed_zero(q);
-        direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked);
+        if (kAsyncDepth > 0) async_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked, stage);
+        else direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked);
         packed_fold(q, st);
         const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
         warp_merge(st, a.c);
@@ -773,6 +841,11 @@ eb_status geometry(int *grid_out, int kind)
         if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return fail(EB_ERR_CUDA, "cudaDeviceGetAttribute failed");
+        if ((cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess ||
+             cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess))
+            return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
         (void)smem_optin;
         // one CTA of kDirectWarps warps per SM; every warp is one unit of the row partition
         g.grid[ebk::kF32Vec] = nsm * ebk::kDirectWarps;
@@ -1051,11 +1124,11 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     // G counts warps (partition units); whole CTAs of kDirectWarps warps, the tail ones idle
     case ebk::kF32Vec:
         ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>
-            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, 0, stream>>>(a1);
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
         break;
     case ebk::kBF16Vec:
         ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>
-            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, 0, stream>>>(a1);
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
         break;
     case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
     default: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;

@@ -131,9 +131,10 @@ def recorded_traffic():
         return None
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+        line = line.strip().lstrip("-* ")
+        if ":" in line and line.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
             k, v = line.split(":", 1)
-            vals[k.strip().strip("-* `")] = v.strip().strip("`")
+            vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_sha256") != src_hash:
         return None
     try:

@@ -384,7 +384,9 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
     __syncthreads();
     if (a.weighted && blockIdx.x == 0)
         for (int r = tid; r <= a.rows; r += blockDim.x) a.prefix_out[r] = P[r];
-    const int gw = blockIdx.x * kDirectWarps + warp;
+    // units are dealt round-robin over the CTAs, so every SM runs a mix of masked (ALU-heavy)
+    // and unmasked (memory-heavy) row pieces rather than one kind
+    const int gw = warp * gridDim.x + blockIdx.x;
     const Partition part{P, a.nvec_row, a.rows, a.weighted};
     SegmentCursor cur;
     cur.begin(part, gw, a.G);

@@ -18,6 +18,8 @@ EB_OK, EB_ERR_INVALID, EB_ERR_CUDA, EB_ERR_UNSUPPORTED, EB_ERR_WORKSPACE, EB_ERR
 EB_F32, EB_BF16 = 0, 1
 EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
+EB_STATUS_TIMEOUT = 0x200
+EB_FLAG_DIAG_STALL = 1
 
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",

@@ -53,6 +53,7 @@ constexpr int kMaxGrid = 8192;
 constexpr int kWeightUnmasked = 11;                // relative cost of a vector of an unmasked row
 constexpr int kWeightMasked = 26;                  // ... and of a masked row (measured 2.36 : 1)
 constexpr uint32_t kWaitLimit = 1u << 26;           // mbarrier polls before giving up
+constexpr uint32_t kDiagWaitLimit = 1u << 12;       // ... under the diagnostic stall flag
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -591,12 +592,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// Waits until the barrier's phase with parity `parity` has completed; false after kWaitLimit
+// Waits until the barrier's phase with parity `parity` has completed; false after `limit`
 // unsuccessful polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit)
 {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"

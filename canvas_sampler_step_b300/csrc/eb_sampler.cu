@@ -995,7 +995,8 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
                        size_t ws_needed)
 {
     if (!params) return fail(EB_ERR_INVALID, "params is NULL");
-    if (params->flags != 0) return fail(EB_ERR_INVALID, "params->flags must be 0");
+    if ((params->flags & ~(uint32_t)EB_FLAG_DIAG_STALL) != 0)
+        return fail(EB_ERR_INVALID, "params->flags has unknown bits 0x%x", params->flags);
     if (params->max_steps < 1) return fail(EB_ERR_INVALID, "max_steps must be >= 1");
     if (!(params->t_start > 0.0f) || !(params->t_end > 0.0f) || !std::isfinite(params->t_start) ||
         !std::isfinite(params->t_end))
@@ -1192,6 +1193,8 @@ eb_status launch_unembed(const eb_params *params, int B, int L, int K, int V, co
     a.c = ebk::kLog2e / T;
     a.invT = 1.0f / T;
     a.keys = round_keys(params ? params->seed : 0);
+    a.stall_first = (params && (params->flags & EB_FLAG_DIAG_STALL)) ? 1 : 0;
+    a.wait_limit = a.stall_first ? ebk::kDiagWaitLimit : ebk::kWaitLimit;
     cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
     g_profile_begin = g_profile_end = nullptr;
     if (prof_begin && record_profile_event(prof_begin, stream) != cudaSuccess)

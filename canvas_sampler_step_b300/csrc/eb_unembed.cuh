@@ -122,6 +122,8 @@ struct Args {
     float c;                    // log2(e) / T
     float invT;
     RoundKeys keys;
+    uint32_t wait_limit;        // mbarrier polls before a wait gives up
+    int stall_first;            // diagnostic: the first operand load of each CTA is withheld
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -191,10 +193,11 @@ __device__ __forceinline__ void tc_wait32(uint32_t (&r)[32])
 }
 
 // Bounded wait that also gives up as soon as another role raised the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag)
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                              uint32_t limit)
 {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -338,24 +341,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m0 = tl.mb * BM, n0 = tl.n * BN;
                 for (int kb = 0; kb < a.KB; ++kb) {
                     const int s = (int)(it % kStages);
-                    if (it >= (uint32_t)kStages && !wait_or_abort(&empty[s], ((it / kStages) & 1u) ^ 1u, abort_flag)) {
+                    if (it >= (uint32_t)kStages &&
+                        !wait_or_abort(&empty[s], ((it / kStages) & 1u) ^ 1u, abort_flag, a.wait_limit)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t st = sbase + (uint32_t)(Smem::ring + (size_t)s * kStageBytes);
-                    const uint32_t fb = smem_addr(&full[s]);
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
-                    tma_load_2d(st, &tmap_h, kb * BK, m0, fb);
+                    if (!(a.stall_first && it == 0)) {
+                        const uint32_t st = sbase + (uint32_t)(Smem::ring + (size_t)s * kStageBytes);
+                        const uint32_t fb = smem_addr(&full[s]);
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+                        tma_load_2d(st, &tmap_h, kb * BK, m0, fb);
 #pragma unroll
-                    for (int i = 0; i < BN / 64; ++i)
-                        tma_load_2d(st + kABytes + i * kBBoxBytes, &tmap_w, n0 + 64 * i, kb * BK, fb);
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_2d(st + kABytes + i * kBBoxBytes, &tmap_w, n0 + 64 * i, kb * BK, fb);
+                    }
                     ++it;
                 }
                 tl.advance();
             }
             // every issued copy has landed before the CTA can leave
             const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
-            for (uint32_t q = first; q < it; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+            for (uint32_t q = first; q < it; ++q)
+                if (!(a.stall_first && q == 0)) mbar_wait(&full[q % kStages], (q / kStages) & 1u, a.wait_limit);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -365,12 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (; ok && tl.valid();) {
                 const uint32_t acc = ti & 1u, use = ti >> 1;
-                if (ti >= 2 && !wait_or_abort(&tempty[acc], (use & 1u) ^ 1u, abort_flag)) break;
+                if (ti >= 2 && !wait_or_abort(&tempty[acc], (use & 1u) ^ 1u, abort_flag, a.wait_limit)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * BN;
                 for (int kb = 0; kb < a.KB; ++kb) {
                     const int s = (int)(it % kStages);
-                    if (!wait_or_abort(&full[s], (it / kStages) & 1u, abort_flag)) {
+                    if (!wait_or_abort(&full[s], (it / kStages) & 1u, abort_flag, a.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // all MMAs issued by this thread are complete before TMEM is released
             tc_commit(smem_addr(drain));
-            mbar_wait(drain, 0);
+            mbar_wait(drain, 0, a.wait_limit);
         }
         __syncwarp();
     } else {
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = ti & 1u, use = ti >> 1;
             // one lane waits; the outcome is warp-uniform, as tcgen05.ld needs the whole warp
             int got = 0;
-            if (ok && lane == 0) got = wait_or_abort(&tfull[acc], use & 1u, abort_flag) ? 1 : 0;
+            if (ok && lane == 0) got = wait_or_abort(&tfull[acc], use & 1u, abort_flag, a.wait_limit) ? 1 : 0;
             ok = ok && __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
             tc_fence_after();
             if (ok) {

@@ -72,9 +72,18 @@ typedef struct {
     float t_end;           /* 0.4: temperature at step max_steps - 1 */
     float entropy_bound;   /* 0.1 */
     float stop_entropy;    /* 0.005 (strict <) */
-    uint32_t flags;        /* reserved, must be 0 */
+    uint32_t flags;        /* 0, or EB_FLAG_DIAG_STALL; other bits are refused */
     uint64_t seed;         /* Philox key (low, high 32 bits) of the Gumbel noise */
 } eb_params;
+
+/* Diagnostic bit of eb_params.flags.  The fused unembedding kernel of eb_unembed_sample then
+ * withholds its first operand load and lets each device wait poll only a few thousand times.
+ * Its bounded waits therefore give up: the kernel waits for the copies it did issue, frees its
+ * tensor memory and returns, and every running canvas of the call ends with EB_STATUS_TIMEOUT
+ * (and EB_STATUS_NONFINITE, as its statistics are empty) while the CUDA context stays usable.
+ * It exists to exercise that failure path without a fault; the other entry points ignore it.
+ * The model card has no counterpart. */
+#define EB_FLAG_DIAG_STALL 1u
 
 /* Fills *p with the model card's recommended settings (48, 0.8, 0.4, 0.1, 0.005) and
  * seed 0.  Returns EB_ERR_INVALID on NULL. */

@@ -96,8 +96,8 @@ def test_invalid_arguments_rejected_before_launch(libs, kw, status):
 
 
 def test_invalid_params_rejected(libs):
-    for field, value in (("max_steps", 0), ("t_start", 0.0), ("t_end", -1.0), ("flags", 1),
-                         ("entropy_bound", float("inf"))):
+    for field, value in (("max_steps", 0), ("t_start", 0.0), ("t_end", -1.0), ("flags", 2),
+                         ("flags", 0x80000001), ("entropy_bound", float("inf"))):
         p = eb.eb_default_params()
         setattr(p, field, value)
         with pytest.raises(eb.EbError) as ei:

@@ -183,3 +183,28 @@ def test_unembed_rejects_bad_shapes():
     with pytest.raises(eb.EbError) as ei:
         c2.unembed_step(gp, h2, W2, 16, 0, 0.8)  # V not a multiple of 8
     assert ei.value.status == eb.EB_ERR_INVALID
+
+
+def test_unembed_stalled_load_times_out_and_context_survives():
+    """Failure detection without a fault: with the diagnostic flag the fused kernel withholds its
+    first operand load, so its bounded waits give up.  The canvases must come back halted with
+    the timeout status and nothing committed, and the same context must then run the normal
+    fused step to oracle parity."""
+    B, L, K, V = 2, 64, 256, 4096
+    u = eb_synth.Unembed(B, L, K, V, seed=3)
+    h, W = _dev(u.h()), _dev(u.W())
+    gp, _ = params_pair(seed=3)
+    gp.flags = eb.EB_FLAG_DIAG_STALL
+    c = eb.Canvas(B, L, V, eb.EB_BF16)
+    c.unembed_step(gp, h, W, K, 0, 0.8)
+    g = host_state(c)                       # synchronises: the kernel returned on its own
+    assert ((g["status"] & eb.EB_STATUS_TIMEOUT) != 0).all()
+    assert (g["selected"] == 0).all() and (g["committed"] == 0).all()
+    assert (g["mask"] == 1).all()           # nothing was unmasked
+    assert (g["steps_taken"] == 1).all()
+    # the next call on the same context is unaffected
+    mask = np.ones((B, L), np.uint8)
+    rep, _, _ = _fused_vs_oracle(B, L, K, V, mask, seed=3)
+    assert rep.max_h_err < H_TOL
+    assert rep.canvas_ties <= 1
+

@@ -568,6 +568,136 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
     consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
 }
 
+// Largest of N floats (N = 4, 8 or 16) with three-input maxima.
+template <int N>
+__device__ __forceinline__ float vec_max(const float (&x)[N])
+{
+    if constexpr (N == 4) {
+        return max3(x[0], x[1], fmaxf(x[2], x[3]));
+    } else if constexpr (N == 8) {
+        return max3(max3(x[0], x[1], x[2]), max3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+    } else {
+        static_assert(N == 16, "vec_max: N is 4, 8 or 16");
+        const float m0 = max3(x[0], x[1], x[2]), m1 = max3(x[3], x[4], x[5]), m2 = max3(x[6], x[7], x[8]);
+        const float m3 = max3(x[9], x[10], x[11]), m4 = max3(x[12], x[13], x[14]);
+        return max3(max3(m0, m1, m2), m3, fmaxf(m4, x[15]));
+    }
+}
+
+// U whole vectors of one lane of a warp that streams one row: vector u holds the VEC entries
+// from (jv0 + 32 u) VEC on.  The arithmetic per entry is that of consume_vals (the warp shares
+// one running maximum and one best Gumbel score), but a whole batch takes one new-maximum vote
+// and, for a masked row, one candidate vote.  The Philox blocks of all U vectors are drawn
+// first, in the same basic block as the unpacking and the maximum, so that their independent
+// chains overlap with the rest.
+template <int VEC, int U, bool MASKED>
+__device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0, const K1Args &a, uint32_t p,
+                                              uint32_t sw, f32x2 c2, RowState &st, PackedSums &q, float &nb,
+                                              f32x2 &nb2, float &K)
+{
+    constexpr int N = U * VEC;
+    float x[N];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if constexpr (VEC == 8) {
+            const uint32_t w4[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[8 * u + 2 * i] = __uint_as_float(w4[i] << 16);
+                x[8 * u + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+            }
+        } else {
+            x[4 * u + 0] = __uint_as_float(r[u].x);
+            x[4 * u + 1] = __uint_as_float(r[u].y);
+            x[4 * u + 2] = __uint_as_float(r[u].z);
+            x[4 * u + 3] = __uint_as_float(r[u].w);
+        }
+    }
+    uint32_t w[MASKED ? N : 1];
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < VEC / 4; ++k) {
+                const uint4 g = philox((jv0 + 32u * (uint32_t)u) * (uint32_t)(VEC / 4) + (uint32_t)k, p,
+                                       (uint32_t)a.step, sw, a.keys);
+                w[VEC * u + 4 * k + 0] = g.x;
+                w[VEC * u + 4 * k + 1] = g.y;
+                w[VEC * u + 4 * k + 2] = g.z;
+                w[VEC * u + 4 * k + 3] = g.w;
+            }
+    }
+    const float vmax = vec_max<N>(x);
+    if (__any_sync(0xFFFFFFFFu, vmax > st.xm)) {
+        float wm = vmax;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+        // first entry holding it: this lane's entries grow with the vector, then the entry, and
+        // all of the warp's vector u precede its vector u + 1
+        int idx = 0x7FFFFFFF;
+        if (vmax == wm) {
+#pragma unroll
+            for (int i = N - 1; i >= 0; --i)
+                if (x[i] == wm) idx = (int)((jv0 + 32u * (uint32_t)(i / VEC)) * (uint32_t)VEC + (uint32_t)(i % VEC));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
+        const float d = (st.xm - wm) * a.c;
+        packed_rescale(q, d, ex2(d));
+        st.ai = idx;
+        st.xm = wm;
+        nb = -wm * a.c;
+        nb2 = pk2(nb, nb);
+        if (MASKED) K = cand_scale(st.xm, st.best, a.c);
+    }
+    float e[N];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const f32x2 tp = fma2(pk2(x[2 * i], x[2 * i + 1]), c2, nb2);
+        float t0, t1;
+        upk2(tp, t0, t1);
+        e[2 * i] = ex2(t0);
+        e[2 * i + 1] = ex2(t1);
+        const f32x2 ep = pk2(e[2 * i], e[2 * i + 1]);
+        if (i & 1) {
+            q.S1 = add2(q.S1, ep);
+            q.T1 = fma2(tp, ep, q.T1);
+        } else {
+            q.S0 = add2(q.S0, ep);
+            q.T0 = fma2(tp, ep, q.T0);
+        }
+    }
+    if constexpr (MASKED) {
+        bool cand[U];
+        bool any = false;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            cand[u] = false;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                cand[u] |= one_minus_u_plus(w[VEC * u + j]) < fmaf(e[VEC * u + j], K, kCandAdd);
+            any |= cand[u];
+        }
+        if (__any_sync(0xFFFFFFFFu, any)) {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (cand[u]) {
+                    const float4 xa = make_float4(x[VEC * u], x[VEC * u + 1], x[VEC * u + 2], x[VEC * u + 3]);
+                    const float4 xb = VEC == 8 ? make_float4(x[VEC * u + (VEC > 4 ? 4 : 0)], x[VEC * u + (VEC > 5 ? 5 : 0)],
+                                                             x[VEC * u + (VEC > 6 ? 6 : 0)], x[VEC * u + (VEC > 7 ? 7 : 0)])
+                                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    const GumbelBest g = gumbel_exact_group<VEC>(
+                        xa, xb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
+                        a.keys.k[0], a.keys.k[1], GumbelBest{st.best, st.bi});
+                    st.best = g.score;
+                    st.bi = g.idx;
+                }
+            warp_best(st.best, st.bi);
+            K = cand_scale(st.xm, st.best, a.c);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- mbarrier / bulk copy PTX
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)

@@ -302,21 +302,13 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
     }
 }
 
-// --- the same segment with a deeper prefetch: each lane copies the vectors it will consume
-// with cp.async (16 bytes each, L2 evict-first, no L1) into its own shared-memory slots,
-// kAsyncDepth batches ahead, and waits only for its own oldest group (no cross-lane barrier).
+// --- the same segment through per-lane cp.async staging (async_segment below)
 #ifndef EB_ASYNC_DEPTH
 #define EB_ASYNC_DEPTH 4
 #endif
 constexpr int kAsyncDepth = EB_ASYNC_DEPTH;
 constexpr int kDirectStageBytes = kAsyncDepth * kDirectU * kDirectThreads * 16;
 
-__device__ __forceinline__ void cp_async16(uint4 *dst, const uint4 *src, uint64_t policy)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "l"(policy)
-                 : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait()
@@ -324,41 +316,92 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const uint4 *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr)
+                 : "memory");
+    return r;
+}
+
+// The nfull whole batches of a segment starting at vector j0.  The thread's staging slot for
+// ring position d and vector u is at sbase + d kDepthStride + u kSlotStride; the ring offset
+// and the global pointer advance by constants, so that no slot or address is recomputed from
+// the batch index.
+template <int VEC, int U, bool MASKED>
+__device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t nfull,
+                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                              float &nb, f32x2 &nb2, float &K, uint32_t sbase)
+{
+    constexpr uint32_t kBatch = 32u * U;
+    constexpr uint32_t kSlotStride = kDirectThreads * 16u;
+    constexpr uint32_t kDepthStride = U * kSlotStride;
+    constexpr uint32_t kRing = kAsyncDepth * kDepthStride;
+    static_assert((kRing & (kRing - 1)) == 0, "the staging ring must be a power of two bytes");
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t pol = evict_first_policy();
+    const uint4 *g = src + j0 + lane;
+#pragma unroll
+    for (int k = 0; k < kAsyncDepth - 1; ++k) {
+        if ((uint32_t)k < nfull)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                cp_async16_at(sbase + (uint32_t)k * kDepthStride + (uint32_t)u * kSlotStride, g + k * kBatch + 32 * u,
+                              pol);
+        cp_async_commit();
+    }
+    const uint4 *gn = g + (kAsyncDepth - 1) * kBatch;        // next batch to prefetch
+    uint32_t off = 0;                                        // ring offset of the batch consumed next
+    uint32_t jv = j0 + lane;
+    // batches b < nfull - (depth - 1) still prefetch batch b + depth - 1
+    const uint32_t npre = nfull > (uint32_t)(kAsyncDepth - 1) ? nfull - (uint32_t)(kAsyncDepth - 1) : 0u;
+    for (uint32_t b = 0; b < nfull; ++b) {
+        if (b < npre) {
+            const uint32_t offn = (off + (uint32_t)(kAsyncDepth - 1) * kDepthStride) & (kRing - 1);
+#pragma unroll
+            for (int u = 0; u < U; ++u) cp_async16_at(sbase + offn + (uint32_t)u * kSlotStride, gn + 32 * u, pol);
+        }
+        cp_async_commit();
+        gn += kBatch;
+        cp_async_wait<kAsyncDepth - 1>();
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = lds128(sbase + off + (uint32_t)u * kSlotStride);
+        consume_batch<VEC, U, MASKED>(r, jv, a, p, sw, c2, st, q, nb, nb2, K);
+        off = (off + kDepthStride) & (kRing - 1);
+        jv += kBatch;
+    }
+    cp_async_wait<0>();
+}
+
+// One row segment [j0, j1) of a warp with a deep prefetch: each lane copies the vectors it
+// will consume with cp.async (16 bytes each, L2 evict-first, no L1) into its own
+// shared-memory slots, kAsyncDepth batches ahead, and waits only for its own oldest group (no
+// cross-lane barrier).  Whole batches run in a masked or an unmasked instance of the loop; the
+// ragged remainder takes plain guarded loads.
 template <int VEC, int U>
 __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
                                               uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
                                               bool gumbel, uint4 *stage)
 {
     constexpr uint32_t kBatch = 32u * U;
-    const uint32_t tid = threadIdx.x, lane = tid & 31;
+    const uint32_t lane = threadIdx.x & 31;
     float nb = -st.xm * a.c;
     f32x2 nb2 = pk2(nb, nb);
     float K = cand_scale(st.xm, st.best, a.c);
     const uint32_t nfull = (j1 - j0) / kBatch;
     const uint32_t jf = j0 + nfull * kBatch;
-    const uint64_t pol = evict_first_policy();
-    // stage layout [depth][U][thread]: consecutive lanes read consecutive 16-byte slots
-    auto slot = [&](uint32_t b, int u) { return stage + ((b % kAsyncDepth) * U + u) * kDirectThreads + tid; };
-#pragma unroll
-    for (int k = 0; k < kAsyncDepth - 1; ++k) {
-        if ((uint32_t)k < nfull)
-#pragma unroll
-            for (int u = 0; u < U; ++u) cp_async16(slot(k, u), src + j0 + k * kBatch + lane + 32u * u, pol);
-        cp_async_commit();
+    const uint32_t sbase = smem_addr(stage) + threadIdx.x * 16u;
+    if (nfull > 0) {
+        if (gumbel) async_batches<VEC, U, true>(a, src, j0, nfull, p, sw, c2, st, q, nb, nb2, K, sbase);
+        else async_batches<VEC, U, false>(a, src, j0, nfull, p, sw, c2, st, q, nb, nb2, K, sbase);
     }
-    for (uint32_t b = 0; b < nfull; ++b) {
-        const uint32_t bn = b + kAsyncDepth - 1;
-        if (bn < nfull)
-#pragma unroll
-            for (int u = 0; u < U; ++u) cp_async16(slot(bn, u), src + j0 + bn * kBatch + lane + 32u * u, pol);
-        cp_async_commit();
-        cp_async_wait<kAsyncDepth - 1>();
-        const uint32_t jb = j0 + b * kBatch;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            consume_packed<VEC, true>(*slot(b, u), true, jb + lane + 32u * u, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
-    }
-    cp_async_wait<0>();
 #pragma unroll 1
     for (uint32_t jb = jf; jb < j1; jb += 32u) {
         const uint32_t idx = jb + lane;

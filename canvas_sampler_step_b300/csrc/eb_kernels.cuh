@@ -360,23 +360,17 @@ struct GumbelBest {
     int idx;
 };
 
-// The rare exact pass over a group of N logits (entries v0 ..) whose group test passed: every
-// entry with 1 - u < 2^t K takes the exact score z - ln(-ln u), and the best one so far is
-// returned.  Kept out of line so that the unrolled hot loop stays small; it recomputes the
-// uniforms and 2^t from the logits.
+// The rare exact pass over a group of N logits (entries v0 ..) whose candidate test passed:
+// every entry with 1 - u < 2^t K takes the exact score z - ln(-ln u), and the best one so far
+// is returned.  The caller passes the entries' Philox words (wa: entries 0-3, wb: 4-7), so
+// nothing is drawn twice; 2^t is recomputed from the logits.  Kept out of line so that the
+// unrolled hot loops stay small.
 template <int N>
-__device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint32_t v0, float c, float invT,
-                                                      float nb, float K, uint32_t p, uint32_t step,
-                                                      uint32_t sw, uint32_t k0, uint32_t k1, GumbelBest best)
+__device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint4 wa, uint4 wb, uint32_t v0,
+                                                      float c, float invT, float nb, float K, GumbelBest best)
 {
     const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    uint32_t w[8];
-    const uint4 u0 = philox_seed(v0 >> 2, p, step, sw, k0, k1);
-    w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
-    if (N == 8) {
-        const uint4 u1 = philox_seed((v0 >> 2) + 1, p, step, sw, k0, k1);
-        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
-    }
+    const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
     for (int j = 0; j < N; ++j) {
         const float e = ex2(fmaf(x[j], c, nb));
@@ -390,6 +384,19 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
         }
     }
     return best;
+}
+
+// The same exact pass for callers that no longer hold the Philox words (the per-thread-row
+// epilogue of the fused kernel, where keeping them live across the vote costs registers): the
+// group's blocks are drawn again from the counter (v0 / 4, p, step, sw) and the seed words.
+template <int N>
+__device__ __noinline__ GumbelBest gumbel_exact_draw(float4 xa, float4 xb, uint32_t v0, float c, float invT,
+                                                     float nb, float K, uint32_t p, uint32_t step, uint32_t sw,
+                                                     uint32_t k0, uint32_t k1, GumbelBest best)
+{
+    const uint4 wa = philox_seed(v0 >> 2, p, step, sw, k0, k1);
+    const uint4 wb = N == 8 ? philox_seed((v0 >> 2) + 1, p, step, sw, k0, k1) : make_uint4(0u, 0u, 0u, 0u);
+    return gumbel_exact_group<N>(xa, xb, wa, wb, v0, c, invT, nb, K, best);
 }
 
 // N = 8 or 4 consecutive logits x of a canvas row, entries v0 .. v0+N-1 (v0 a multiple of
@@ -504,11 +511,12 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
         bool cand = false;
         if (valid && gumbel) {
             const uint4 u0 = philox(v0 >> 2, p, (uint32_t)a.step, sw, a.keys);
+            uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
 #if EB_GROUP_TEST
             float fmin = min3(one_minus_u_plus(u0.x), one_minus_u_plus(u0.y),
                               fminf(one_minus_u_plus(u0.z), one_minus_u_plus(u0.w)));
             if constexpr (N == 8) {
-                const uint4 u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
+                u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
                 fmin = min3(fmin, min3(one_minus_u_plus(u1.x), one_minus_u_plus(u1.y), one_minus_u_plus(u1.z)),
                             one_minus_u_plus(u1.w));
             }
@@ -516,11 +524,8 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
             const float emax = ex2(fmaf(vmax, a.c, nb));
             cand = fmin < fmaf(emax, K, kCandAdd);
 #else
-            uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, 0u, 0u, 0u, 0u};
-            if constexpr (N == 8) {
-                const uint4 u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
-                w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
-            }
+            if constexpr (N == 8) u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
             for (int j = 0; j < N; ++j) cand |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
 #endif
@@ -532,9 +537,8 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                 const float4 xb = N == 8 ? make_float4(x[N > 4 ? 4 : 0], x[N > 5 ? 5 : 0], x[N > 6 ? 6 : 0],
                                                        x[N > 7 ? 7 : 0])
                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                const GumbelBest g = gumbel_exact_group<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
-                                                           a.keys.k[0], a.keys.k[1],
-                                                           GumbelBest{st.best, st.bi});
+                const GumbelBest g = gumbel_exact_draw<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
+                                                          a.keys.k[0], a.keys.k[1], GumbelBest{st.best, st.bi});
                 st.best = g.score;
                 st.bi = g.idx;
             }
@@ -686,9 +690,12 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
                     const float4 xb = VEC == 8 ? make_float4(x[VEC * u + (VEC > 4 ? 4 : 0)], x[VEC * u + (VEC > 5 ? 5 : 0)],
                                                              x[VEC * u + (VEC > 6 ? 6 : 0)], x[VEC * u + (VEC > 7 ? 7 : 0)])
                                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    const GumbelBest g = gumbel_exact_group<VEC>(
-                        xa, xb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
-                        a.keys.k[0], a.keys.k[1], GumbelBest{st.best, st.bi});
+                    const uint4 wa = make_uint4(w[VEC * u], w[VEC * u + 1], w[VEC * u + 2], w[VEC * u + 3]);
+                    const uint4 wb = VEC == 8 ? make_uint4(w[VEC * u + (VEC > 4 ? 4 : 0)], w[VEC * u + (VEC > 5 ? 5 : 0)],
+                                                           w[VEC * u + (VEC > 6 ? 6 : 0)], w[VEC * u + (VEC > 7 ? 7 : 0)])
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                    const GumbelBest g = gumbel_exact_group<VEC>(xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC,
+                                                                 a.c, a.invT, nb, K, GumbelBest{st.best, st.bi});
                     st.best = g.score;
                     st.bi = g.idx;
                 }

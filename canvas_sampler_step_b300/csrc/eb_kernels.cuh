@@ -355,6 +355,20 @@ __device__ __forceinline__ uint4 philox_seed(uint32_t c0, uint32_t c1, uint32_t 
     return make_uint4(c0, c1, c2, c3);
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128w(uint32_t addr)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr)
+                 : "memory");
+    return r;
+}
+
 struct GumbelBest {
     float score;
     int idx;
@@ -401,23 +415,22 @@ __device__ __noinline__ GumbelBest gumbel_exact_draw(float4 xa, float4 xb, uint3
 
 // N = 8 or 4 consecutive logits x of a canvas row, entries v0 .. v0+N-1 (v0 a multiple of
 // N): running max / first argmax, S and T2 (on packed f32x2 pairs when EB_PACKED is 1), and
-// for masked rows the Gumbel candidate test, done once per group: the smallest 1 - u of its
-// entries against the largest 2^t.  `a` supplies c = log2(e)/T, invT = 1/T, the step and the
-// Philox round keys.  WARP_ROW: the 32 lanes work on the same row (they share the best score
-// when it moves, so every lane must call this with the same trip count; `valid` masks lanes
-// without a group); otherwise every lane owns its row.  `gumbel` (runtime) switches the
-// sampling part off for a lane whose row is not masked.
+// for masked rows the per-entry Gumbel candidate test 1 - u < 2^t K, whose rare passes take
+// the exact score.  `a` supplies c = log2(e)/T, invT = 1/T, the step and the Philox round
+// keys.  WARP_ROW: the 32 lanes work on the same row (they share the best score when it
+// moves, so every lane must call this with the same trip count; `valid` masks lanes without a
+// group); otherwise every lane owns its row.  `gumbel` (runtime) switches the sampling part
+// off for a lane whose row is not masked.  `stash` (per-thread rows only) is the shared address
+// of a 32-byte slot of this thread that keeps a candidate group's Philox words for the exact
+// pass; with WARP_ROW the pass draws them again.
 #ifndef EB_PACKED
 #define EB_PACKED 1
-#endif
-#ifndef EB_GROUP_TEST
-#define EB_GROUP_TEST 0
 #endif
 template <int N, bool MASKED, bool WARP_ROW, typename Args>
 __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, uint32_t v0, const Args &a,
                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
                                              PackedSums &q, float &nb, f32x2 &nb2, float &K,
-                                             bool gumbel = true)
+                                             bool gumbel = true, uint32_t stash = 0u)
 {
     float vmax = 0.0f;
     float e[N];
@@ -512,23 +525,16 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
         if (valid && gumbel) {
             const uint4 u0 = philox(v0 >> 2, p, (uint32_t)a.step, sw, a.keys);
             uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-#if EB_GROUP_TEST
-            float fmin = min3(one_minus_u_plus(u0.x), one_minus_u_plus(u0.y),
-                              fminf(one_minus_u_plus(u0.z), one_minus_u_plus(u0.w)));
-            if constexpr (N == 8) {
-                u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
-                fmin = min3(fmin, min3(one_minus_u_plus(u1.x), one_minus_u_plus(u1.y), one_minus_u_plus(u1.z)),
-                            one_minus_u_plus(u1.w));
-            }
-            // 2^t is largest at the group's maximum: one test bounds all N entries
-            const float emax = ex2(fmaf(vmax, a.c, nb));
-            cand = fmin < fmaf(emax, K, kCandAdd);
-#else
             if constexpr (N == 8) u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
             const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
             for (int j = 0; j < N; ++j) cand |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
-#endif
+            // a candidate's words go to the thread's shared slot, so that they need not stay
+            // live in registers across the vote nor be drawn again
+            if (!WARP_ROW && cand) {
+                sts128(stash, u0);
+                sts128(stash + 16u, u1);
+            }
         }
         const bool go = __any_sync(WARP_ROW ? 0xFFFFFFFFu : __activemask(), cand);
         if (go) {
@@ -537,8 +543,13 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                 const float4 xb = N == 8 ? make_float4(x[N > 4 ? 4 : 0], x[N > 5 ? 5 : 0], x[N > 6 ? 6 : 0],
                                                        x[N > 7 ? 7 : 0])
                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                const GumbelBest g = gumbel_exact_draw<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw,
-                                                          a.keys.k[0], a.keys.k[1], GumbelBest{st.best, st.bi});
+                GumbelBest g;
+                if constexpr (!WARP_ROW)
+                    g = gumbel_exact_group<N>(xa, xb, lds128w(stash), lds128w(stash + 16u), v0, a.c, a.invT, nb, K,
+                                              GumbelBest{st.best, st.bi});
+                else
+                    g = gumbel_exact_draw<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw, a.keys.k[0],
+                                             a.keys.k[1], GumbelBest{st.best, st.bi});
                 st.best = g.score;
                 st.bi = g.idx;
             }

@@ -105,7 +105,8 @@ struct Smem {
     static constexpr size_t drain = tempty + 2 * 8;
     static constexpr size_t tmem_base = drain + 8;
     static constexpr size_t abort_flag = tmem_base + 4;
-    static constexpr size_t total = abort_flag + 4;
+    static constexpr size_t stash = (abort_flag + 4 + 15) & ~(size_t)15;  // 32 B per epilogue thread
+    static constexpr size_t total = stash + (size_t)kEpiWarps * 32 * 32;
     static constexpr size_t alloc = total + 1024;                         // alignment slack
 };
 
@@ -253,7 +254,7 @@ struct Tiles {
 // `gumbel` is off for lanes whose row is not masked).
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], int v0, bool on, bool gumbel, const Args &a,
                                           uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
-                                          float &nb, f32x2 &nb2, float &K)
+                                          float &nb, f32x2 &nb2, float &K, uint32_t stash)
 {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -261,7 +262,8 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], int v0, bool 
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[8 * g + j]);
         const int vg = v0 + 8 * g;
-        consume_vals<8, true, false>(x, on && vg < a.V, (uint32_t)vg, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+        consume_vals<8, true, false>(x, on && vg < a.V, (uint32_t)vg, a, p, sw, c2, st, q, nb, nb2, K, gumbel,
+                                     stash);
     }
 }
 
@@ -406,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hh = (warp - 2) >> 2;            // accumulator column group
         const int rl = 32 * q + lane;              // row within the block
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(hh * kEpiCols);
+        const uint32_t stash = sbase + (uint32_t)Smem::stash + (uint32_t)(tid - 64) * 32u;
         uint32_t ti = 0;
         bool ok = true;
         int cur_mb = -1;
@@ -458,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_ld32(base + (uint32_t)(32 * (ch + 1)), rb);
                     const int v0 = vbase + 32 * ch;
                     if (LOGITS) store_logits(ra, cur_mb * BM + rl, v0, a);
-                    else epi_chunk(ra, v0, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K);
+                    else epi_chunk(ra, v0, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K, stash);
                     tc_wait32(rb);
                     if (ch + 2 < kEpiCols / 32) tc_ld32(base + (uint32_t)(32 * (ch + 2)), ra);
                     if (LOGITS) store_logits(rb, cur_mb * BM + rl, v0 + 32, a);
-                    else epi_chunk(rb, v0 + 32, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K);
+                    else epi_chunk(rb, v0 + 32, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K, stash);
                     if (ch + 2 < kEpiCols / 32) tc_wait32(ra);
                 }
             }

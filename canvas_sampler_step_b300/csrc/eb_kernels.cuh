@@ -685,12 +685,18 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
     if constexpr (MASKED) {
         bool cand[U];
         bool any = false;
+        // the threshold 2^t K + (1 + 2^-23) of two entries at a time
+        const f32x2 K2 = pk2(K, K), A2 = pk2(kCandAdd, kCandAdd);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             cand[u] = false;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                cand[u] |= one_minus_u_plus(w[VEC * u + j]) < fmaf(e[VEC * u + j], K, kCandAdd);
+            for (int j = 0; j < VEC; j += 2) {
+                float h0, h1;
+                upk2(fma2(pk2(e[VEC * u + j], e[VEC * u + j + 1]), K2, A2), h0, h1);
+                cand[u] |= one_minus_u_plus(w[VEC * u + j]) < h0;
+                cand[u] |= one_minus_u_plus(w[VEC * u + j + 1]) < h1;
+            }
             any |= cand[u];
         }
         if (__any_sync(0xFFFFFFFFu, any)) {

@@ -61,10 +61,11 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("single", "fused", "loop"), default="single",
+    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop"), default="single",
                     help="single: the single-step workload (default, the headline line); fused: "
-                         "the fused unembedding + sampler step (4 x 256 positions, K=2048); loop: "
-                         "the adaptive 48-step loop over 8 canvases with the stand-in denoiser")
+                         "the fused unembedding + sampler step (4 x 256 positions, K=2048); "
+                         "fused1: the same for one canvas (256 positions); loop: the adaptive "
+                         "48-step loop over 8 canvases with the stand-in denoiser")
     return ap.parse_args(argv)
 
 
@@ -560,10 +561,9 @@ def run_reference(args, rank, world, local):
 
 # ------------------------------------------------------------------ fused unembedding workload
 
-FUSED_METRIC = ("EB-sampler fused unembedding steps/s at 4x256 positions, K=2048, V=262144 bf16; "
+FUSED_METRIC = ("EB-sampler fused unembedding steps/s at {B}x256 positions, K=2048, V=262144 bf16; "
                 "achieved tensor TFLOP/s vs B300 peak")
-FB, FL, FK, FV = 4, 256, 2048, 262144
-FUSED_FLOP = 2 * FB * FL * FK * FV
+FL, FK, FV = 256, 2048, 262144
 
 
 def measured_tensor_peak():
@@ -576,10 +576,10 @@ def measured_tensor_peak():
 
 
 def run_fused(args, rank, world, local):
-    """One step = eb_unembed_sample over 1024 fresh all-masked positions: h [1024, 2048] x
-    W [2048, 262144] on the tensor cores, the row statistics in the epilogue, the selection.
-    h and W are resident (W is the model's unembedding matrix); each graph replay restores
-    the canvas states first."""
+    """One step = eb_unembed_sample over B x 256 fresh all-masked positions (B = 4, or 1 for
+    the small-batch workload): h [256 B, 2048] x W [2048, 262144] on the tensor cores, the row
+    statistics in the epilogue, the selection.  h and W are resident (W is the model's
+    unembedding matrix); each graph replay restores the canvas states first."""
     import ctypes
 
     import torch
@@ -587,6 +587,8 @@ def run_fused(args, rank, world, local):
     import canvas_sampler_step_b300 as eb
     import eb_synth.device as synth_dev
 
+    FB = 1 if args.workload == "fused1" else 4
+    FUSED_FLOP = 2 * FB * FL * FK * FV
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
@@ -686,13 +688,13 @@ def run_fused(args, rank, world, local):
     h2d = h_host.numel() * 2 + sum(v.numel() * v.element_size() for v in hstate.values())
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
     out = {
-        "metric": FUSED_METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+        "metric": FUSED_METRIC.format(B=FB), "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": slowest * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Philox / Box-Muller h and W, eb_synth)",
-        "config": {"workload": "fused unembedding + EB sampler step: h [1024, 2048] ~ N(0,1) x W "
+        "config": {"workload": f"fused unembedding + EB sampler step: h [{FB * FL}, 2048] ~ N(0,1) x W "
                                "[2048, 262144] ~ N(0, 0.02^2) + 0.05 planted per row, bf16, "
-                               "4 canvases x 256 positions all masked, T=0.8",
+                               f"{FB} canvas{'es' if FB > 1 else ''} x 256 positions all masked, T=0.8",
                    "B": FB, "L": FL, "K": FK, "V": FV,
                    "l2": "W (1 GiB) > 126 MB L2, read once per step",
                    "launch": f"CUDA graph of {N} steps (+ canvas-state restores) replayed {R} times",
@@ -792,7 +794,7 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
-    elif args.workload == "fused":
+    elif args.workload in ("fused", "fused1"):
         run_fused(args, rank, world, local)
     elif args.workload == "loop":
         run_loop(args, rank, world, local)

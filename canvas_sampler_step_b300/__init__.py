@@ -20,6 +20,8 @@ EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
 EB_STATUS_TIMEOUT = 0x200
 EB_FLAG_DIAG_STALL = 1
+EB_FLAG_STOP_MASKED_ONLY = 2
+EB_FLAG_FINALIZE_SAMPLED = 4
 
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",

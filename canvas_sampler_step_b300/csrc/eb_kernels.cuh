@@ -137,6 +137,9 @@ struct K2Args {
     float c;
     long long bound_q;         // entropy_bound in 2^-40 nats (rounded down)
     long long stop_q;          // stop_entropy * L in 2^-40 nats (rounded up): mean < stop
+    double stop_entropy;       // for the masked-only statistics (threshold per masked count)
+    int stop_masked_only;      // EB_FLAG_STOP_MASKED_ONLY
+    int finalize_sampled;      // EB_FLAG_FINALIZE_SAMPLED
     int k3_g;                  // > 0: partials come from the fused unembedding kernel, whose
                                // row block mb, group rank j < k3_g and column group hh <
                                // k3_groups write slot ((mb k3_g + j) k3_groups + hh) 128 + row % 128

@@ -644,8 +644,11 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         a.entropy[r] = H;
         a.argmax[r] = A;
         a.sampled[r] = Y;
-        my_sum += hq;
-        my_unstable |= (Pv[p] != A) ? 1 : 0;
+        // the stop statistics: every position, or the still-masked ones only
+        if (m || !a.stop_masked_only) {
+            my_sum += hq;
+            my_unstable |= (Pv[p] != A) ? 1 : 0;
+        }
         if (m) {
             ++my_masked;
             if ((long long)hq <= a.bound_q) {
@@ -672,7 +675,10 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         bigmin = red_min[w] < bigmin ? red_min[w] : bigmin;
     }
     const int nm = n_masked, ns = n_small;
-    const float mean = (float)((double)sumq / 1099511627776.0 / (double)L);
+    const int nstat = a.stop_masked_only ? nm : L;
+    const float mean = nstat > 0 ? (float)((double)sumq / 1099511627776.0 / (double)nstat) : NAN;
+    const long long stop_q =
+        a.stop_masked_only ? (long long)ceil(a.stop_entropy * (double)nstat * 1099511627776.0) : a.stop_q;
     if (bad_flags) {
         if (tid == 0) {
             a.status[b] = ((bad_flags & 1) ? EB_STATUS_NONFINITE : 0) | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
@@ -683,7 +689,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         for (int p = tid; p < L; p += blockDim.x) a.selected[rowbase + p] = 0;
         return;
     }
-    const bool stop = a.step >= 1 && stable && (long long)sumq < a.stop_q;
+    const bool stop = a.step >= 1 && stable && nstat > 0 && (long long)sumq < stop_q;
 
     if (stop) {
         // adaptive stop: every still-masked position takes its argmax
@@ -798,11 +804,11 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const long long r = rowbase + p;
         uint8_t sel = 0;
         if (Acc[p]) {
-            a.tokens[r] = stop ? As[p] : Ys[p];
+            a.tokens[r] = (stop && !a.finalize_sampled) ? As[p] : Ys[p];
             a.mask[r] = 0;
             sel = 1;
         } else if (Ms[p] && new_status == EB_STOP_CAP) {
-            a.tokens[r] = As[p];
+            a.tokens[r] = a.finalize_sampled ? Ys[p] : As[p];
             a.mask[r] = 0;
             sel = 1;
         }
@@ -1038,7 +1044,7 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
                        size_t ws_needed)
 {
     if (!params) return fail(EB_ERR_INVALID, "params is NULL");
-    if ((params->flags & ~(uint32_t)EB_FLAG_DIAG_STALL) != 0)
+    if ((params->flags & ~(uint32_t)(EB_FLAG_DIAG_STALL | EB_FLAG_STOP_MASKED_ONLY | EB_FLAG_FINALIZE_SAMPLED)) != 0)
         return fail(EB_ERR_INVALID, "params->flags has unknown bits 0x%x", params->flags);
     if (params->max_steps < 1) return fail(EB_ERR_INVALID, "max_steps must be >= 1");
     if (!(params->t_start > 0.0f) || !(params->t_end > 0.0f) || !std::isfinite(params->t_start) ||
@@ -1099,6 +1105,9 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     // fixed point, 2^-40 nats: accept while prefix <= floor(bound), stop while sum < ceil(stop L)
     a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
     a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
+    a2.stop_entropy = (double)params->stop_entropy;
+    a2.stop_masked_only = (params->flags & EB_FLAG_STOP_MASKED_ONLY) ? 1 : 0;
+    a2.finalize_sampled = (params->flags & EB_FLAG_FINALIZE_SAMPLED) ? 1 : 0;
     a2.k3_g = k3_g;
     a2.k3_groups = ebk::k3::kEpiGroups;
     // programmatic dependent launch: the selection grid is set up while the row-statistics

@@ -72,9 +72,21 @@ typedef struct {
     float t_end;           /* 0.4: temperature at step max_steps - 1 */
     float entropy_bound;   /* 0.1 */
     float stop_entropy;    /* 0.005 (strict <) */
-    uint32_t flags;        /* 0, or EB_FLAG_DIAG_STALL; other bits are refused */
+    uint32_t flags;        /* 0 or EB_FLAG_* bits below; other bits are refused */
     uint64_t seed;         /* Philox key (low, high 32 bits) of the Gumbel noise */
 } eb_params;
+
+/* Reading variants (bits of eb_params.flags).  The model card leaves two points of the stop
+ * rule open; the default reading (flags 0) is: the mean entropy and the argmax-stability test
+ * run over all L positions, committed ones included ("mean model entropy over the whole
+ * canvas", DiffusionGemma model card, Best practices section 1, adaptive stop), and positions
+ * still masked at an adaptive stop or at the step cap take the current argmax.
+ *   EB_FLAG_STOP_MASKED_ONLY: the stop statistics run over the positions still masked at the
+ *     start of the step (mean_entropy then reports that mean);
+ *   EB_FLAG_FINALIZE_SAMPLED: positions finalised at an adaptive stop or at the step cap take
+ *     their sampled token instead of the argmax. */
+#define EB_FLAG_STOP_MASKED_ONLY 2u
+#define EB_FLAG_FINALIZE_SAMPLED 4u
 
 /* Diagnostic bit of eb_params.flags.  The fused unembedding kernel of eb_unembed_sample then
  * withholds its first operand load and lets each device wait poll only a few thousand times.

@@ -21,7 +21,9 @@ run_loop(...)              -- the <= 48-step denoising loop with per-canvas stop
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py`` except the
 readings the pages leave open (shaped-entropy stop statistic, mean over all positions,
-argmax finalisation at stop / cap), which are "parity unpinned" by the pages.
+argmax finalisation at stop / cap), which are "parity unpinned" by the pages.  The two
+alternative readings selectable by ``Params.flags`` (stop statistics over the masked positions
+only, sampled-token finalisation) are pinned by hand-built cases like the default ones.
 """
 from __future__ import annotations
 
@@ -77,6 +79,7 @@ def _load():
     lib.eb_oracle_select.restype = ctypes.c_int
     lib.eb_oracle_step.argtypes = [ctypes.c_int, ctypes.c_int, i64, ctypes.c_int, P,
                                    ctypes.c_int, f64, ctypes.c_int, f64, f64, f64, f64, u64,
+                                   ctypes.c_uint32,
                                    P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.eb_oracle_step.restype = None
     lib.eb_oracle_num_threads.argtypes = []
@@ -171,6 +174,12 @@ class Params:
     entropy_bound: float = 0.1
     stop_entropy: float = 0.005
     seed: int = 0
+    flags: int = 0            # reading variants: STOP_MASKED_ONLY, FINALIZE_SAMPLED
+
+
+# Reading variants of the stop / finalisation rules (Params.flags bits)
+STOP_MASKED_ONLY = 2          # stop statistics over the still-masked positions only
+FINALIZE_SAMPLED = 4          # positions finalised at stop / cap take the sampled token
 
 
 @dataclass
@@ -231,7 +240,7 @@ def step(logits: np.ndarray, state: State, step_index: int, params: Params = Par
     stm = np.zeros(B, np.float64)
     _load().eb_oracle_step(B, L, V, dt, _ptr(x), int(step_index), float(temperature),
                            params.max_steps, params.t_start, params.t_end, params.entropy_bound,
-                           params.stop_entropy, params.seed,
+                           params.stop_entropy, params.seed, params.flags,
                            _ptr(st.mask), _ptr(st.tokens), _ptr(st.prev_argmax), _ptr(st.status),
                            _ptr(st.steps_taken), _ptr(H), _ptr(A), _ptr(Y), _ptr(gap), _ptr(sel),
                            _ptr(committed), _ptr(meanH), _ptr(sm), _ptr(om), _ptr(stm))

@@ -247,6 +247,15 @@ int eb_oracle_select(int L, const double *H, const uint8_t *mask, double bound,
     return k;
 }
 
+/* Reading variants (bits of `flags` in eb_oracle_step; the values match the library's
+ * parameter flags, an interface convention only):
+ *   STOP_MASKED_ONLY  the stop rule's mean entropy and its argmax-stability test run over
+ *                     the positions still masked at the start of the step, instead of all L;
+ *   FINALIZE_SAMPLED  on adaptive stop and at the step cap the positions still masked take
+ *                     their sampled token Y instead of the argmax A. */
+#define ORACLE_FLAG_STOP_MASKED_ONLY 2u
+#define ORACLE_FLAG_FINALIZE_SAMPLED 4u
+
 /* One full EB sampler step over B canvases of L positions (logits [B, L, V]).
  *
  * State (in/out): mask [B*L] (1 = still masked), tokens [B*L] (-1 while masked),
@@ -259,11 +268,11 @@ int eb_oracle_select(int L, const double *H, const uint8_t *mask, double bound,
  * Order within a step: row statistics -> stop test (s >= 1) -> on stop, every masked
  * position takes its argmax; otherwise selection and commit of the sampled tokens, then
  * the complete / cap check (at the cap the rest take their argmax) -> prev_argmax = A.
- * temperature <= 0 selects the linear schedule. */
+ * temperature <= 0 selects the linear schedule; flags selects the reading variants above. */
 void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
                     int step, double temperature,
                     int max_steps, double t_start, double t_end, double bound,
-                    double stop_entropy, uint64_t seed,
+                    double stop_entropy, uint64_t seed, uint32_t flags,
                     uint8_t *mask, int32_t *tokens, int32_t *prev_argmax,
                     int32_t *status, int32_t *steps_taken,
                     double *H, int32_t *A, int32_t *Y, double *gap, uint8_t *selected,
@@ -295,20 +304,25 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
         if (stop_margin) stop_margin[b] = INFINITY;
         if (status[b] != EB_ORACLE_RUNNING) continue;
         int64_t base = (int64_t)b * L;
+        const int masked_only = (flags & ORACLE_FLAG_STOP_MASKED_ONLY) != 0;
+        const int fin_sampled = (flags & ORACLE_FLAG_FINALIZE_SAMPLED) != 0;
         double sumH = 0.0;
+        int nstat = 0;
         int stable = 1;
         for (int p = 0; p < L; ++p) {
+            if (masked_only && !mask[base + p]) continue;
             sumH += H[base + p];
+            ++nstat;
             if (A[base + p] != prev_argmax[base + p]) stable = 0;
         }
-        double meanH = sumH / (double)L;
+        double meanH = nstat > 0 ? sumH / (double)nstat : NAN;
         if (mean_entropy) mean_entropy[b] = meanH;
-        if (stop_margin && step >= 1 && stable) stop_margin[b] = fabs(meanH - stop_entropy);
+        if (stop_margin && step >= 1 && stable && nstat > 0) stop_margin[b] = fabs(meanH - stop_entropy);
         int count = 0;
-        if (step >= 1 && stable && meanH < stop_entropy) {
+        if (step >= 1 && stable && nstat > 0 && meanH < stop_entropy) {
             for (int p = 0; p < L; ++p) {
                 if (mask[base + p]) {
-                    tokens[base + p] = A[base + p];
+                    tokens[base + p] = fin_sampled ? Y[base + p] : A[base + p];
                     mask[base + p] = 0;
                     selected[base + p] = 1;
                     ++count;
@@ -338,7 +352,7 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
             } else if (step >= max_steps - 1) {
                 for (int p = 0; p < L; ++p) {
                     if (mask[base + p]) {
-                        tokens[base + p] = A[base + p];
+                        tokens[base + p] = fin_sampled ? Y[base + p] : A[base + p];
                         mask[base + p] = 0;
                         selected[base + p] = 1;
                         ++count;

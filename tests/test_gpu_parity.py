@@ -407,3 +407,63 @@ def test_resume_reproduces_uninterrupted_run():
     a, b = host_state(full), host_state(part)
     for k in ("tokens", "status", "steps_taken", "prev_argmax"):
         assert np.array_equal(a[k], b[k]), k
+
+
+# ---------------------------------------------------------------- reading variants (flags)
+
+def _variant_step(x, flags, step=1, mask=None, prev=None, **prm):
+    B, L, V = x.shape
+    gp, op = params_pair(seed=13, flags=flags, **prm)
+    c = eb.Canvas(B, L, V, eb.EB_F32, mask=mask)
+    ost = oracle.State.fresh(B, L, mask)
+    if prev is not None:
+        c.prev_argmax.copy_(torch.as_tensor(prev, dtype=torch.int32))
+        ost.prev_argmax[:] = prev
+    c.step(gp, to_device_logits(x), step, 0.0)
+    g = host_state(c)
+    res = oracle.step(x, ost, step, op)
+    rep = Report()
+    compare_step(g, res, ost, np.ones(B, bool), rep, ctx=f"flags {flags}")
+    return g, res, ost, rep
+
+
+def test_stop_masked_only_parity():
+    """Committed positions with uniform rows (H = ln V) and a changed argmax block the default
+    stop; with EB_FLAG_STOP_MASKED_ONLY only the still-masked, sharply peaked positions count,
+    so the canvases stop.  GPU and oracle agree under both readings."""
+    B, L, V = 2, 64, 512
+    x = np.zeros((B, L, V), np.float32)
+    peak = (np.arange(L) * 7 + 3) % V
+    for b in range(B):
+        x[b, np.arange(L), peak] = 40.0
+    mask = np.ones((B, L), np.uint8)
+    mask[:, : L // 2] = 0
+    x[:, : L // 2, :] = 0.0
+    prev = np.broadcast_to(np.where(np.arange(L) < L // 2, 5, peak), (B, L)).astype(np.int32)
+    g, res, ost, _ = _variant_step(x, 0, mask=mask, prev=prev, entropy_bound=-1.0)
+    assert (g["status"] == eb.EB_RUNNING).all() and (ost.status == oracle.RUNNING).all()
+    g, res, ost, _ = _variant_step(x, eb.EB_FLAG_STOP_MASKED_ONLY, mask=mask, prev=prev, entropy_bound=-1.0)
+    assert (g["status"] == eb.EB_STOP_ADAPTIVE).all() and (ost.status == oracle.ADAPTIVE).all()
+    assert (g["mean_entropy"] < 1e-6).all()
+    assert np.array_equal(g["tokens"], ost.tokens)
+
+
+def test_finalize_sampled_parity_at_stop_and_cap():
+    """EB_FLAG_FINALIZE_SAMPLED: the positions an adaptive stop or the step cap finalises take
+    the sampled token; GPU and oracle agree, and the tokens differ from the argmax."""
+    B, L, V = 2, 48, 512
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((B, L, V)) * 0.5).astype(np.float32)
+    probe = oracle.State.fresh(B, L)
+    r0 = oracle.step(x, probe, 1, params_pair(seed=13)[1])
+    g, res, ost, rep = _variant_step(x, eb.EB_FLAG_FINALIZE_SAMPLED, prev=r0.A, stop_entropy=100.0)
+    assert (g["status"] == eb.EB_STOP_ADAPTIVE).all()
+    assert (g["tokens"] == g["sampled"]).all()
+    assert (g["tokens"] != g["argmax"]).sum() >= 10
+    cfg = eb_synth.Peaked(1, 16, 512, "f32", 3.0, 0.0, 0.0, (0.0,), (31,))
+    rep, hist, c = _lockstep(cfg, params_kw={"entropy_bound": -1.0, "max_steps": 5,
+                                             "flags": eb.EB_FLAG_FINALIZE_SAMPLED})
+    last = hist[-1]
+    assert last["status"][0] == eb.EB_STOP_CAP
+    fin = last["selected"][0].astype(bool)
+    assert (last["tokens"][0][fin] == last["sampled"][0][fin]).all()

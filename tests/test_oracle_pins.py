@@ -362,3 +362,59 @@ def test_bf16_to_f64_exact():
     vals = oracle.bf16_to_f64(bits)
     assert vals[0] == 1.0 and vals[1] == -1.0 and vals[2] == 0.0
     assert vals[3] == 3.140625 and vals[4] == float(np.float32(3.3895313892515355e38))
+
+
+# ---------------------------------------------------------------- reading variants (flags)
+
+def test_masked_only_stop_statistics_ignore_committed_positions():
+    """STOP_MASKED_ONLY: the mean entropy and the argmax-stability test run over the positions
+    still masked.  Committed positions with uniform rows (H = ln 16) and a changed argmax block
+    the default stop but not the variant."""
+    B, L, V = 1, 8, 16
+    x = _peaked(B, L, V, [[p + 8 for p in range(L)]])
+    x[0, :4, :] = 0.0                                # committed positions: uniform, H = ln 16
+    st0 = oracle.State.fresh(B, L)
+    st0.mask[0, :4] = 0
+    st0.tokens[0, :4] = 3
+    st0.prev_argmax[0, :] = [5, 5, 5, 5, 12, 13, 14, 15]   # A = 0 at the uniform rows
+    runs = {}
+    for flags in (0, oracle.STOP_MASKED_ONLY):
+        st = st0.copy()
+        r = oracle.step(x, st, 1, oracle.Params(flags=flags, entropy_bound=-1.0))
+        runs[flags] = (st, r)
+    st, r = runs[0]
+    assert st.status[0] == oracle.RUNNING
+    assert r.mean_entropy[0] == pytest.approx(4 * np.log(16) / 8, rel=1e-12)
+    st, r = runs[oracle.STOP_MASKED_ONLY]
+    assert st.status[0] == oracle.ADAPTIVE and st.steps_taken[0] == 2
+    assert r.mean_entropy[0] < 1e-12
+    assert st.tokens[0].tolist() == [3, 3, 3, 3, 12, 13, 14, 15]
+
+
+def test_finalize_sampled_takes_the_sampled_token_at_stop_and_cap():
+    """FINALIZE_SAMPLED: positions finalised by the adaptive stop or the step cap take Y, the
+    Gumbel-max sample, instead of the argmax A."""
+    B, L, V = 1, 12, 10
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((B, L, V)) * 0.5).astype(np.float32)
+    # adaptive stop at step 1 (threshold above every mean, argmax stable)
+    for flags, key in ((0, "A"), (oracle.FINALIZE_SAMPLED, "Y")):
+        probe = oracle.State.fresh(B, L)
+        r0 = oracle.step(x, probe, 1, oracle.Params(stop_entropy=0.0))
+        st = oracle.State.fresh(B, L)
+        st.prev_argmax[:] = r0.A
+        r = oracle.step(x, st, 1, oracle.Params(stop_entropy=100.0, flags=flags))
+        assert st.status[0] == oracle.ADAPTIVE
+        assert (st.tokens == getattr(r, key)).all()
+        assert (r.Y != r.A).sum() >= 3          # the two readings differ here
+    # cap after three one-position steps
+    for flags, key in ((0, "A"), (oracle.FINALIZE_SAMPLED, "Y")):
+        st = oracle.State.fresh(B, L)
+        prm = oracle.Params(max_steps=3, entropy_bound=-1.0, flags=flags)
+        for s in range(3):
+            r = oracle.step(x + np.float32(s), st, s, prm)
+        assert st.status[0] == oracle.CAP
+        fin = r.selected[0].astype(bool)
+        assert fin.sum() == L - 2
+        assert (st.tokens[0][fin] == getattr(r, key)[0][fin]).all()
+        assert (r.Y[0][fin] != r.A[0][fin]).sum() >= 3

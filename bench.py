@@ -61,11 +61,12 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop"), default="single",
+    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "blocks"), default="single",
                     help="single: the single-step workload (default, the headline line); fused: "
                          "the fused unembedding + sampler step (4 x 256 positions, K=2048); "
                          "fused1: the same for one canvas (256 positions); loop: the adaptive "
-                         "48-step loop over 8 canvases with the stand-in denoiser")
+                         "48-step loop over 8 canvases with the stand-in denoiser; blocks: the "
+                         "block driver, 64 blocks on 8 slots")
     return ap.parse_args(argv)
 
 
@@ -714,6 +715,81 @@ def run_fused(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ block driver workload
+
+BLOCKS_METRIC = ("EB block driver (continuous batching): blocks/s over 64 blocks x 256 x 262144 bf16 "
+                 "on 8 slots, stand-in denoiser included")
+
+
+def run_blocks(args, rank, world, local):
+    """eb_sample_blocks: 64 blocks (peak growth 0.1-0.8, so they stop after different step
+    counts) on 8 slots; a freed slot takes the next block while the others keep denoising.
+    The stand-in denoiser regenerates the occupied slots' logits on the device every iteration."""
+    import ctypes
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth
+    import eb_synth.device as synth_dev
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    eb.lib()
+    synth_dev.lib()
+    stream = torch.cuda.current_stream(device)
+    n, slots = 64, 8
+    cfg = eb_synth.cfg3(B=n)
+    recipe = synth_dev.Recipe.of(cfg)
+    buf = torch.empty((slots, cfg.L, cfg.V), dtype=torch.int16, device=device)
+    ws_bytes = eb.eb_blocks_workspace_bytes(slots, cfg.L, cfg.V, eb.EB_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    toks = torch.empty((n, cfg.L), dtype=torch.int32, device=device)
+    steps = torch.empty(n, dtype=torch.int32, device=device)
+    status = torch.empty(n, dtype=torch.int32, device=device)
+    params = eb.eb_default_params(seed=0)
+
+    def drive():
+        return eb.eb_sample_blocks(params, slots, cfg.L, cfg.V, eb.EB_BF16, synth_dev.block_callback_address(),
+                                   ctypes.addressof(recipe), buf, n, toks, steps, status, ws, ws_bytes,
+                                   poll_every=8)
+
+    drive()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        iters = drive()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, local)
+    elapsed = start.elapsed_time(end) / 1e3
+    value, slowest = aggregate(n, elapsed, world, dist, local)
+    st = steps.cpu().numpy()
+    out = {
+        "metric": BLOCKS_METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": n,
+        "warmup": 1, "ms_per_step": slowest * 1e3 / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Philox / Box-Muller stand-in denoiser, eb_synth)",
+        "config": {"workload": "block driver: 64 blocks x 256 positions x 262144 bf16, sigma 3, peak "
+                               "U(0,4) + r s, r in (0.1, 0.2, 0.4, 0.8), up to 48 steps each, 8 slots",
+                   "slots": slots, "iterations": iters, "parallelism": f"replicas x{world}"},
+        "canvas_steps_per_s": float(st.sum()) / slowest,
+        "slot_occupancy": float(st.sum()) / (iters * slots),
+        "steps_to_stop_mean": float(st.mean()),
+        "stop_reasons": {str(k): int(v) for k, v in zip(*np.unique(status.cpu().numpy(), return_counts=True))},
+        "gpu_launches": None,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ adaptive loop workload
 
 LOOP_METRIC = ("EB adaptive denoising loop: canvas-steps/s over 8 canvases x 256 x 262144 bf16 "
@@ -798,6 +874,8 @@ def main(argv=None):
         run_fused(args, rank, world, local)
     elif args.workload == "loop":
         run_loop(args, rank, world, local)
+    elif args.workload == "blocks":
+        run_blocks(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 

@@ -19,6 +19,7 @@ EB_F32, EB_BF16 = 0, 1
 EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
 EB_STATUS_TIMEOUT = 0x200
+EB_SLOT_IDLE = 0x400
 EB_FLAG_DIAG_STALL = 1
 EB_FLAG_STOP_MASKED_ONLY = 2
 EB_FLAG_FINALIZE_SAMPLED = 4
@@ -26,7 +27,7 @@ EB_FLAG_FINALIZE_SAMPLED = 4
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",
             "eb_unembed_workspace_bytes", "eb_unembed_sample", "eb_unembed_logits",
-            "eb_sampler_step_noalloc")
+            "eb_sampler_step_noalloc", "eb_blocks_workspace_bytes", "eb_sample_blocks")
 
 
 class EbParams(ctypes.Structure):
@@ -88,6 +89,11 @@ def lib() -> ctypes.CDLL:
     L.eb_sampler_step_noalloc.argtypes = ([ctypes.POINTER(EbParams), i32, i32, i32, i32, P, i32,
                                            ctypes.c_float] + [P] * 11 + [P])
     L.eb_sampler_step_noalloc.restype = i32
+    L.eb_blocks_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.eb_blocks_workspace_bytes.restype = sz
+    L.eb_sample_blocks.argtypes = ([ctypes.POINTER(EbParams), i32, i32, i32, i32, P, P, P, i32, P, P, P,
+                                    P, sz, i32, ctypes.POINTER(ctypes.c_int), P])
+    L.eb_sample_blocks.restype = i32
     _lib = L
     return L
 
@@ -159,6 +165,24 @@ def eb_sample_canvas(params: EbParams, B: int, L: int, V: int, dtype: int, logit
                                   _ptr(entropy), _ptr(argmax), _ptr(sampled), _ptr(selected),
                                   _ptr(workspace), workspace_bytes, poll_every,
                                   ctypes.byref(ran), _stream(stream)))
+    return ran.value
+
+
+def eb_blocks_workspace_bytes(B: int, L: int, V: int, dtype: int) -> int:
+    return int(lib().eb_blocks_workspace_bytes(B, L, V, dtype))
+
+
+def eb_sample_blocks(params: EbParams, B: int, L: int, V: int, dtype: int, logits_fn, user, logits,
+                     n_blocks: int, block_tokens, block_steps, block_status, workspace,
+                     workspace_bytes: int, poll_every: int = 0, stream=None) -> int:
+    """Block driver over B slots; ``logits_fn`` is a C function address of an
+    eb_block_logits_fn.  Returns the number of iterations enqueued."""
+    fn = logits_fn if isinstance(logits_fn, int) else ctypes.cast(logits_fn, ctypes.c_void_p).value
+    ran = ctypes.c_int(0)
+    _check(lib().eb_sample_blocks(ctypes.byref(params), B, L, V, dtype, fn, _ptr(user), _ptr(logits),
+                                  n_blocks, _ptr(block_tokens), _ptr(block_steps), _ptr(block_status),
+                                  _ptr(workspace), workspace_bytes, poll_every, ctypes.byref(ran),
+                                  _stream(stream)))
     return ran.value
 
 

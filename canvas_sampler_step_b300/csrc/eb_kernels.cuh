@@ -108,6 +108,12 @@ struct K1Args {
     float c;                // log2(e) / T
     float invT;             // 1 / T
     RoundKeys keys;
+    // per-canvas overrides of step, c and 1/T and the canvas id of the Philox counter, or null
+    // (continuous batching: every slot's canvas is at its own step)
+    const int32_t *canvas_step;
+    const int32_t *canvas_id;
+    const float *canvas_c;
+    const float *canvas_invT;
 };
 
 struct K2Args {
@@ -138,6 +144,8 @@ struct K2Args {
     long long bound_q;         // entropy_bound in 2^-40 nats (rounded down)
     long long stop_q;          // stop_entropy * L in 2^-40 nats (rounded up): mean < stop
     double stop_entropy;       // for the masked-only statistics (threshold per masked count)
+    const int32_t *canvas_step;  // per-canvas step, or null (then `step`)
+    const float *canvas_c;       // per-canvas c, or null (then `c`)
     int stop_masked_only;      // EB_FLAG_STOP_MASKED_ONLY
     int finalize_sampled;      // EB_FLAG_FINALIZE_SAMPLED
     int k3_g;                  // > 0: partials come from the fused unembedding kernel, whose
@@ -416,6 +424,13 @@ __device__ __noinline__ GumbelBest gumbel_exact_draw(float4 xa, float4 xb, uint3
     return gumbel_exact_group<N>(xa, xb, wa, wb, v0, c, invT, nb, K, best);
 }
 
+// Per-row values of the arithmetic: c = log2(e) / T and 1 / T of the row's canvas, the
+// canvas's step and the row's Philox counter words (position p, stream and canvas id sw).
+struct RowCtx {
+    float c, invT;
+    uint32_t step, p, sw;
+};
+
 // N = 8 or 4 consecutive logits x of a canvas row, entries v0 .. v0+N-1 (v0 a multiple of
 // N): running max / first argmax, S and T2 (on packed f32x2 pairs when EB_PACKED is 1), and
 // for masked rows the per-entry Gumbel candidate test 1 - u < 2^t K, whose rare passes take
@@ -431,7 +446,7 @@ __device__ __noinline__ GumbelBest gumbel_exact_draw(float4 xa, float4 xb, uint3
 #endif
 template <int N, bool MASKED, bool WARP_ROW, typename Args>
 __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, uint32_t v0, const Args &a,
-                                             uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                             const RowCtx &rc, f32x2 c2, RowState &st,
                                              PackedSums &q, float &nb, f32x2 &nb2, float &K,
                                              bool gumbel = true, uint32_t stash = 0u)
 {
@@ -462,17 +477,17 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
-            const float d = (st.xm - wm) * a.c;
+            const float d = (st.xm - wm) * rc.c;
             packed_rescale(q, d, ex2(d));
             st.ai = idx;
             st.xm = wm;
-            nb = -wm * a.c;
+            nb = -wm * rc.c;
             nb2 = pk2(nb, nb);
-            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, a.c);
+            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, rc.c);
         }
     } else if (__any_sync(__activemask(), newmax)) {
         if (newmax) {
-                const float d = (st.xm - vmax) * a.c;
+                const float d = (st.xm - vmax) * rc.c;
                 packed_rescale(q, d, ex2(d));
                 int j0 = N - 1;
 #pragma unroll
@@ -480,9 +495,9 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                     if (x[j] == vmax) j0 = j;
                 st.ai = (int)(v0 + (uint32_t)j0);
                 st.xm = vmax;
-                nb = -vmax * a.c;
+                nb = -vmax * rc.c;
                 nb2 = pk2(nb, nb);
-            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, a.c);
+            if (MASKED && gumbel) K = cand_scale(st.xm, st.best, rc.c);
         }
     }
     if (valid) {
@@ -512,7 +527,7 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
         upk2(q.T1, t2[2], t2[3]);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
-            const float t = fmaf(x[j], a.c, nb);
+            const float t = fmaf(x[j], rc.c, nb);
             e[j] = ex2(t);
             s[j & 3] += e[j];
             t2[j & 3] = fmaf(t, e[j], t2[j & 3]);
@@ -526,9 +541,9 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
     if constexpr (MASKED) {
         bool cand = false;
         if (valid && gumbel) {
-            const uint4 u0 = philox(v0 >> 2, p, (uint32_t)a.step, sw, a.keys);
+            const uint4 u0 = philox(v0 >> 2, rc.p, rc.step, rc.sw, a.keys);
             uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (N == 8) u1 = philox((v0 >> 2) + 1, p, (uint32_t)a.step, sw, a.keys);
+            if constexpr (N == 8) u1 = philox((v0 >> 2) + 1, rc.p, rc.step, rc.sw, a.keys);
             const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
             for (int j = 0; j < N; ++j) cand |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
@@ -548,16 +563,16 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 GumbelBest g;
                 if constexpr (!WARP_ROW)
-                    g = gumbel_exact_group<N>(xa, xb, lds128w(stash), lds128w(stash + 16u), v0, a.c, a.invT, nb, K,
+                    g = gumbel_exact_group<N>(xa, xb, lds128w(stash), lds128w(stash + 16u), v0, rc.c, rc.invT, nb, K,
                                               GumbelBest{st.best, st.bi});
                 else
-                    g = gumbel_exact_draw<N>(xa, xb, v0, a.c, a.invT, nb, K, p, (uint32_t)a.step, sw, a.keys.k[0],
+                    g = gumbel_exact_draw<N>(xa, xb, v0, rc.c, rc.invT, nb, K, rc.p, rc.step, rc.sw, a.keys.k[0],
                                              a.keys.k[1], GumbelBest{st.best, st.bi});
                 st.best = g.score;
                 st.bi = g.idx;
             }
             if (WARP_ROW) warp_best(st.best, st.bi);
-            K = cand_scale(st.xm, st.best, a.c);
+            K = cand_scale(st.xm, st.best, rc.c);
         }
     }
 }
@@ -565,7 +580,7 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
 // One 16-byte vector of VEC logits (8 bf16 or 4 fp32) of a row, entries jvec*VEC ..
 template <int VEC, bool MASKED>
 __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32_t jvec, const K1Args &a,
-                                               uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                               const RowCtx &rc, f32x2 c2, RowState &st,
                                                PackedSums &q, float &nb, f32x2 &nb2, float &K,
                                                bool gumbel = true)
 {
@@ -583,7 +598,7 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
         x[2] = __uint_as_float(r.z);
         x[3] = __uint_as_float(r.w);
     }
-    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, rc, c2, st, q, nb, nb2, K, gumbel);
 }
 
 // Largest of N floats (N = 4, 8 or 16) with three-input maxima.
@@ -609,8 +624,8 @@ __device__ __forceinline__ float vec_max(const float (&x)[N])
 // first, in the same basic block as the unpacking and the maximum, so that their independent
 // chains overlap with the rest.
 template <int VEC, int U, bool MASKED>
-__device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0, const K1Args &a, uint32_t p,
-                                              uint32_t sw, f32x2 c2, RowState &st, PackedSums &q, float &nb,
+__device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0, const K1Args &a, const RowCtx &rc,
+                                              f32x2 c2, RowState &st, PackedSums &q, float &nb,
                                               f32x2 &nb2, float &K)
 {
     constexpr int N = U * VEC;
@@ -637,8 +652,8 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
         for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int k = 0; k < VEC / 4; ++k) {
-                const uint4 g = philox((jv0 + 32u * (uint32_t)u) * (uint32_t)(VEC / 4) + (uint32_t)k, p,
-                                       (uint32_t)a.step, sw, a.keys);
+                const uint4 g = philox((jv0 + 32u * (uint32_t)u) * (uint32_t)(VEC / 4) + (uint32_t)k, rc.p,
+                                       rc.step, rc.sw, a.keys);
                 w[VEC * u + 4 * k + 0] = g.x;
                 w[VEC * u + 4 * k + 1] = g.y;
                 w[VEC * u + 4 * k + 2] = g.z;
@@ -660,13 +675,13 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
-        const float d = (st.xm - wm) * a.c;
+        const float d = (st.xm - wm) * rc.c;
         packed_rescale(q, d, ex2(d));
         st.ai = idx;
         st.xm = wm;
-        nb = -wm * a.c;
+        nb = -wm * rc.c;
         nb2 = pk2(nb, nb);
-        if (MASKED) K = cand_scale(st.xm, st.best, a.c);
+        if (MASKED) K = cand_scale(st.xm, st.best, rc.c);
     }
     float e[N];
 #pragma unroll
@@ -715,12 +730,12 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
                                                            w[VEC * u + (VEC > 6 ? 6 : 0)], w[VEC * u + (VEC > 7 ? 7 : 0)])
                                               : make_uint4(0u, 0u, 0u, 0u);
                     const GumbelBest g = gumbel_exact_group<VEC>(xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC,
-                                                                 a.c, a.invT, nb, K, GumbelBest{st.best, st.bi});
+                                                                 rc.c, rc.invT, nb, K, GumbelBest{st.best, st.bi});
                     st.best = g.score;
                     st.bi = g.idx;
                 }
             warp_best(st.best, st.bi);
-            K = cand_scale(st.xm, st.best, a.c);
+            K = cand_scale(st.xm, st.best, rc.c);
         }
     }
 }

@@ -65,11 +65,32 @@ __device__ __forceinline__ void gumbel_words(long long jvec, uint32_t p, uint32_
     }
 }
 
+// The arithmetic values of a row of canvas b at position p: the launch's step and temperature,
+// or the canvas's own when the launch carries per-canvas arrays (continuous batching), whose
+// canvas id then also replaces b in the Philox counter.
+__device__ __forceinline__ RowCtx row_ctx(const K1Args &a, int b, uint32_t p)
+{
+    RowCtx rc;
+    if (a.canvas_step) {
+        rc.c = a.canvas_c[b];
+        rc.invT = a.canvas_invT[b];
+        rc.step = (uint32_t)a.canvas_step[b];
+        rc.sw = (kStreamGumbel << 24) | (uint32_t)a.canvas_id[b];
+    } else {
+        rc.c = a.c;
+        rc.invT = a.invT;
+        rc.step = (uint32_t)a.step;
+        rc.sw = (kStreamGumbel << 24) | (uint32_t)b;
+    }
+    rc.p = p;
+    return rc;
+}
+
 // One vector of VEC logits (entries jvec*VEC ..).  Every lane of the warp calls this with
 // the same trip count; `valid` masks lanes without a vector.
 template <int VEC, bool MASKED>
 __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, long long jvec,
-                                            const K1Args &a, uint32_t p, uint32_t sw,
+                                            const K1Args &a, const RowCtx &rc,
                                             RowState &st, float &nb, float &K)
 {
     float e[VEC];
@@ -80,7 +101,7 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
         else vmax = x[0];
         if (vmax > st.xm) {
             // new running max: rescale the sums and take its first index as the argmax
-            const float d = (st.xm - vmax) * a.c;
+            const float d = (st.xm - vmax) * rc.c;
             const float sc = ex2(d);
             st.T2 = sc == 0.0f ? 0.0f : sc * fmaf(d, st.S, st.T2);
             st.S = sc == 0.0f ? 0.0f : st.S * sc;
@@ -90,12 +111,12 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
                 if (x[j] == vmax) j0 = j;
             st.ai = (int)(jvec * VEC + j0);
             st.xm = vmax;
-            nb = -vmax * a.c;
-            if (MASKED) K = cand_scale(st.xm, st.best, a.c);
+            nb = -vmax * rc.c;
+            if (MASKED) K = cand_scale(st.xm, st.best, rc.c);
         }
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const float t = fmaf(x[j], a.c, nb);
+            const float t = fmaf(x[j], rc.c, nb);
             e[j] = ex2(t);
             st.S += e[j];
             st.T2 = fmaf(t, e[j], st.T2);
@@ -105,7 +126,7 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
         uint32_t w[VEC];
         bool any = false;
         if (valid) {
-            gumbel_words<VEC>(jvec, p, (uint32_t)a.step, sw, a.keys, w);
+            gumbel_words<VEC>(jvec, rc.p, rc.step, rc.sw, a.keys, w);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) any |= one_minus_u_plus(w[j]) < fmaf(e[j], K, kCandAdd);
         }
@@ -117,7 +138,7 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
                     if (f < fmaf(e[j], K, kCandAdd)) {
                         const float delta = f - kOneMinusHalfUlp;          // 1 - u, exact
                         const float E = -log1pf(-delta);                   // -ln u
-                        const float score = x[j] * a.invT - logf(E);
+                        const float score = x[j] * rc.invT - logf(E);
                         const int idx = (int)(jvec * VEC + j);
                         if (better(score, idx, st.best, st.bi)) {
                             st.best = score;
@@ -127,7 +148,7 @@ __device__ __forceinline__ void consume_vec(const float (&x)[VEC], bool valid, l
                 }
             }
             warp_best(st.best, st.bi);
-            K = cand_scale(st.xm, st.best, a.c);
+            K = cand_scale(st.xm, st.best, rc.c);
         }
     }
 }
@@ -196,12 +217,12 @@ __device__ __forceinline__ void write_partial(Partial *dst, const RowState &s, i
 
 // Block reduction of the consumers' states and the partial write (consumer threads only).
 // A NaN in any thread's sums is recorded before the merge can scale it away.
-__device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, RowState *red,
+__device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, float c, RowState *red,
                                                  uint32_t *redflag, int row, int flags)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
-    warp_merge(st, a.c);
+    warp_merge(st, c);
     if (lane == 0) {
         red[warp] = st;
         redflag[warp] = nan_here ? (uint32_t)kPartialNonfinite : 0u;
@@ -210,7 +231,7 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, R
     if (warp == 0) {
         RowState s2 = lane < kConsumerWarps ? red[lane] : empty_state();
         const uint32_t nf = __reduce_or_sync(0xFFFFFFFFu, lane < kConsumerWarps ? redflag[lane] : 0u);
-        warp_merge(s2, a.c);
+        warp_merge(s2, c);
         if (lane == 0) write_partial(&a.partials[row + blockIdx.x], s2, flags | (int)nf);
     }
     consumer_sync();
@@ -254,12 +275,12 @@ __device__ __forceinline__ void load_full(uint4 (&r)[U], const uint4 *src, uint3
 
 template <int VEC, int U>
 __device__ __forceinline__ void consume_full(const uint4 (&r)[U], uint32_t jb, uint32_t lane, const K1Args &a,
-                                             uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                             const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
                                              float &nb, f32x2 &nb2, float &K, bool gumbel)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        consume_packed<VEC, true>(r[u], true, jb + lane + 32u * (uint32_t)u, a, p, sw, c2, st, q, nb, nb2, K,
+        consume_packed<VEC, true>(r[u], true, jb + lane + 32u * (uint32_t)u, a, rc, c2, st, q, nb, nb2, K,
                                   gumbel);
 }
 
@@ -270,14 +291,14 @@ __device__ __forceinline__ void consume_full(const uint4 (&r)[U], uint32_t jb, u
 // the unrolled loop small enough for the instruction cache.
 template <int VEC, int U>
 __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
-                                               uint32_t p, uint32_t sw, f32x2 c2, RowState &st,
+                                               const RowCtx &rc, f32x2 c2, RowState &st,
                                                PackedSums &q, bool gumbel)
 {
     constexpr uint32_t kBatch = 32u * U;
     const uint32_t lane = threadIdx.x & 31;
-    float nb = -st.xm * a.c;
+    float nb = -st.xm * rc.c;
     f32x2 nb2 = pk2(nb, nb);
-    float K = cand_scale(st.xm, st.best, a.c);
+    float K = cand_scale(st.xm, st.best, rc.c);
     const uint32_t jf = j0 + (j1 - j0) / kBatch * kBatch;
     if (jf > j0) {
         uint4 A[U], B[U];
@@ -285,11 +306,11 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
         for (uint32_t jb = j0;; jb += 2 * kBatch) {
             const bool hasB = jb + kBatch < jf;
             if (hasB) load_full<U>(B, src, jb + kBatch, lane);
-            consume_full<VEC, U>(A, jb, lane, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+            consume_full<VEC, U>(A, jb, lane, a, rc, c2, st, q, nb, nb2, K, gumbel);
             if (!hasB) break;
             const bool hasA = jb + 2 * kBatch < jf;
             if (hasA) load_full<U>(A, src, jb + 2 * kBatch, lane);
-            consume_full<VEC, U>(B, jb + kBatch, lane, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+            consume_full<VEC, U>(B, jb + kBatch, lane, a, rc, c2, st, q, nb, nb2, K, gumbel);
             if (!hasA) break;
         }
     }
@@ -298,7 +319,7 @@ __device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src
         const uint32_t idx = jb + lane;
         const bool valid = idx < j1;
         const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-        consume_packed<VEC, true>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+        consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
     }
 }
 
@@ -336,7 +357,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 // the batch index.
 template <int VEC, int U, bool MASKED>
 __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t nfull,
-                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                              const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
                                               float &nb, f32x2 &nb2, float &K, uint32_t sbase)
 {
     constexpr uint32_t kBatch = 32u * U;
@@ -373,7 +394,7 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r[u] = lds128(sbase + off + (uint32_t)u * kSlotStride);
-        consume_batch<VEC, U, MASKED>(r, jv, a, p, sw, c2, st, q, nb, nb2, K);
+        consume_batch<VEC, U, MASKED>(r, jv, a, rc, c2, st, q, nb, nb2, K);
         off = (off + kDepthStride) & (kRing - 1);
         jv += kBatch;
     }
@@ -387,27 +408,27 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
 // ragged remainder takes plain guarded loads.
 template <int VEC, int U>
 __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
-                                              uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                              const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
                                               bool gumbel, uint4 *stage)
 {
     constexpr uint32_t kBatch = 32u * U;
     const uint32_t lane = threadIdx.x & 31;
-    float nb = -st.xm * a.c;
+    float nb = -st.xm * rc.c;
     f32x2 nb2 = pk2(nb, nb);
-    float K = cand_scale(st.xm, st.best, a.c);
+    float K = cand_scale(st.xm, st.best, rc.c);
     const uint32_t nfull = (j1 - j0) / kBatch;
     const uint32_t jf = j0 + nfull * kBatch;
     const uint32_t sbase = smem_addr(stage) + threadIdx.x * 16u;
     if (nfull > 0) {
-        if (gumbel) async_batches<VEC, U, true>(a, src, j0, nfull, p, sw, c2, st, q, nb, nb2, K, sbase);
-        else async_batches<VEC, U, false>(a, src, j0, nfull, p, sw, c2, st, q, nb, nb2, K, sbase);
+        if (gumbel) async_batches<VEC, U, true>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
+        else async_batches<VEC, U, false>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
     }
 #pragma unroll 1
     for (uint32_t jb = jf; jb < j1; jb += 32u) {
         const uint32_t idx = jb + lane;
         const bool valid = idx < j1;
         const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-        consume_packed<VEC, true>(r, valid, idx, a, p, sw, c2, st, q, nb, nb2, K, gumbel);
+        consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
     }
 }
 
@@ -433,25 +454,24 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
     const Partition part{P, a.nvec_row, a.rows, a.weighted};
     SegmentCursor cur;
     cur.begin(part, gw, a.G);
-    const f32x2 c2 = pk2(a.c, a.c);
     int row;
     long long j0, j1;
     while (cur.next(row, j0, j1)) {
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
-        const uint32_t p = (uint32_t)(row - b * a.L);
+        const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
+        const f32x2 c2 = pk2(rc.c, rc.c);
         const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
-        const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
         const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.logits) +
                                                            (size_t)row * (size_t)a.row_bytes);
         RowState st = empty_state();
         PackedSums q;
         packed_zero(q);
-        if (kAsyncDepth > 0) async_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked, stage);
-        else direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, p, sw, c2, st, q, masked);
+        if (kAsyncDepth > 0) async_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, rc, c2, st, q, masked, stage);
+        else direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, rc, c2, st, q, masked);
         packed_fold(q, st);
         const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
-        warp_merge(st, a.c);
+        warp_merge(st, rc.c);
         if (lane == 0) {
             write_partial(&a.partials[row + gw], st, nan_here ? kPartialNonfinite : 0);
             if (cur.first) a.rowunits[row].x = gw;
@@ -482,13 +502,12 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
     while (cur.next(row, j0, j1)) {
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
-        const uint32_t p = (uint32_t)(row - b * a.L);
+        const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
         const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
-        const uint32_t sw = (kStreamGumbel << 24) | (uint32_t)b;
         const char *base = static_cast<const char *>(a.logits) + (size_t)row * (size_t)a.row_bytes;
         RowState st = empty_state();
-        float nb = -st.xm * a.c;
-        float K = cand_scale(st.xm, st.best, a.c);
+        float nb = -st.xm * rc.c;
+        float K = cand_scale(st.xm, st.best, rc.c);
         for (long long j = j0; j < j1; j += kConsumers) {
             const long long v = j + tid;
             const bool valid = v < j1;
@@ -497,10 +516,10 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
                 if (KIND == kF32Scalar) x[0] = __ldg(reinterpret_cast<const float *>(base) + v);
                 else x[0] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(base) + v) << 16);
             }
-            if (masked) consume_vec<1, true>(x, valid, v, a, p, sw, st, nb, K);
-            else consume_vec<1, false>(x, valid, v, a, p, sw, st, nb, K);
+            if (masked) consume_vec<1, true>(x, valid, v, a, rc, st, nb, K);
+            else consume_vec<1, false>(x, valid, v, a, rc, st, nb, K);
         }
-        reduce_and_store(st, a, red, scan, row, 0);
+        reduce_and_store(st, a, rc.c, red, scan, row, 0);
         if (tid == 0) {
             if (cur.first) a.rowunits[row].x = blockIdx.x;
             if (cur.last) a.rowunits[row].y = blockIdx.x;
@@ -564,6 +583,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L;
     if (a.status[b] != EB_RUNNING) return;       // CTA-uniform
+    // the canvas's own step and c under continuous batching, else the launch's
+    const int step = a.canvas_step ? a.canvas_step[b] : a.step;
+    const float cb = a.canvas_c ? a.canvas_c[b] : a.c;
     if (tid == 0) {
         n_masked = 0;
         n_small = 0;
@@ -622,7 +644,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
                     const unsigned long long c = (unsigned long long)(base - r + i0 + k);
                     if (c * W / G >= (c + 1) * W / G) continue;
                 }
-                merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, a.c);
+                merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, cb);
                 flags |= q[k].flags;
             }
         }
@@ -682,14 +704,14 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     if (bad_flags) {
         if (tid == 0) {
             a.status[b] = ((bad_flags & 1) ? EB_STATUS_NONFINITE : 0) | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
-            if (a.steps_taken) a.steps_taken[b] = a.step + 1;
+            if (a.steps_taken) a.steps_taken[b] = step + 1;
             if (a.committed) a.committed[b] = 0;
             if (a.mean_entropy) a.mean_entropy[b] = NAN;
         }
         for (int p = tid; p < L; p += blockDim.x) a.selected[rowbase + p] = 0;
         return;
     }
-    const bool stop = a.step >= 1 && stable && nstat > 0 && (long long)sumq < stop_q;
+    const bool stop = step >= 1 && stable && nstat > 0 && (long long)sumq < stop_q;
 
     if (stop) {
         // adaptive stop: every still-masked position takes its argmax
@@ -798,7 +820,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     int new_status = EB_RUNNING;
     if (stop) new_status = EB_STOP_ADAPTIVE;
     else if (!any_left) new_status = EB_STOP_COMPLETE;
-    else if (a.step >= a.max_steps - 1) new_status = EB_STOP_CAP;
+    else if (step >= a.max_steps - 1) new_status = EB_STOP_CAP;
     int my_commit = 0;
     for (int p = tid; p < L; p += blockDim.x) {
         const long long r = rowbase + p;
@@ -822,12 +844,12 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const int committed = n_committed;
         if (new_status != EB_RUNNING) {
             a.status[b] = new_status;
-            if (a.steps_taken) a.steps_taken[b] = a.step + 1;
+            if (a.steps_taken) a.steps_taken[b] = step + 1;
         }
         if (a.committed) a.committed[b] = committed;
         if (a.mean_entropy) a.mean_entropy[b] = mean;
-        if (a.committed_hist) a.committed_hist[(long long)b * a.max_steps + a.step] = committed;
-        if (a.mean_hist) a.mean_hist[(long long)b * a.max_steps + a.step] = mean;
+        if (a.committed_hist) a.committed_hist[(long long)b * a.max_steps + step] = committed;
+        if (a.mean_hist) a.mean_hist[(long long)b * a.max_steps + step] = mean;
     }
 }
 
@@ -1037,6 +1059,11 @@ struct StepBuffers {
     float *mean_entropy;
     int32_t *committed_hist;
     float *mean_hist;
+    // continuous batching: per-canvas step, Philox canvas id, c and 1/T (all or none)
+    const int32_t *canvas_step = nullptr;
+    const int32_t *canvas_id = nullptr;
+    const float *canvas_c = nullptr;
+    const float *canvas_invT = nullptr;
 };
 
 eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dtype,
@@ -1106,6 +1133,8 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     a2.bound_q = (long long)std::floor((double)params->entropy_bound * 1099511627776.0);
     a2.stop_q = (long long)std::ceil((double)params->stop_entropy * (double)L * 1099511627776.0);
     a2.stop_entropy = (double)params->stop_entropy;
+    a2.canvas_step = sb.canvas_step;
+    a2.canvas_c = sb.canvas_c;
     a2.stop_masked_only = (params->flags & EB_FLAG_STOP_MASKED_ONLY) ? 1 : 0;
     a2.finalize_sampled = (params->flags & EB_FLAG_FINALIZE_SAMPLED) ? 1 : 0;
     a2.k3_g = k3_g;
@@ -1171,6 +1200,10 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a1.c = ebk::kLog2e / T;
     a1.invT = 1.0f / T;
     a1.keys = round_keys(params->seed);
+    a1.canvas_step = sb.canvas_step;
+    a1.canvas_id = sb.canvas_id;
+    a1.canvas_c = sb.canvas_c;
+    a1.canvas_invT = sb.canvas_invT;
     cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
     g_profile_begin = g_profile_end = nullptr;
     if (prof_begin && record_profile_event(prof_begin, stream) != cudaSuccess)
@@ -1442,6 +1475,224 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
         }
     }
     if (steps_run) *steps_run = ran;
+    return ok();
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- block driver
+//
+// Continuous batching over B canvas slots: block k of n is a fresh all-masked canvas whose
+// Philox canvas id is k.  Every iteration the denoiser fills the logits of the occupied slots,
+// one sampler step runs with each slot's own step and temperature, and the refill kernel
+// retires the slots that stopped (their tokens, step count and stop reason go to block k's
+// outputs) and hands them the next block, or leaves them idle when none is left.
+namespace {
+
+struct BlockSlots {
+    uint8_t *mask;
+    int32_t *tokens, *prev_argmax, *status, *steps_taken;
+    float *entropy;
+    int32_t *argmax, *sampled;
+    uint8_t *selected;
+    int32_t *slot_block, *slot_step;
+    float *slot_c, *slot_invT;
+    int32_t *counters;          // [0] next block to hand out, [1] blocks finished
+};
+
+// The schedule temperature of `step` and its c = log2(e) / T and 1 / T, with the same binary32
+// operations, in the same order, as the host's eb_temperature (no contraction).
+__device__ __forceinline__ void slot_temperature(float t_start, float t_end, int max_steps, int step,
+                                                 float *c, float *invT)
+{
+    float T = t_start;
+    if (max_steps > 1)
+        T = __fadd_rn(t_start, __fdiv_rn(__fmul_rn(__fsub_rn(t_end, t_start), (float)step), (float)(max_steps - 1)));
+    *c = __fdiv_rn(ebk::kLog2e, T);
+    *invT = __fdiv_rn(1.0f, T);
+}
+
+__device__ void slot_reset(const BlockSlots &s, int b, int L, int block, float t_start, float t_end,
+                           int max_steps)
+{
+    const long long base = (long long)b * L;
+    for (int p = threadIdx.x; p < L; p += blockDim.x) {
+        s.mask[base + p] = block >= 0 ? 1 : 0;
+        s.tokens[base + p] = -1;
+        s.prev_argmax[base + p] = -1;
+    }
+    if (threadIdx.x == 0) {
+        s.status[b] = block >= 0 ? EB_RUNNING : EB_SLOT_IDLE;
+        s.steps_taken[b] = 0;
+        s.slot_block[b] = block;
+        s.slot_step[b] = 0;
+        slot_temperature(t_start, t_end, max_steps, 0, &s.slot_c[b], &s.slot_invT[b]);
+    }
+}
+
+__global__ void blocks_init(const BlockSlots s, int L, int n_blocks, float t_start, float t_end, int max_steps)
+{
+    const int b = blockIdx.x;
+    slot_reset(s, b, L, b < n_blocks ? b : -1, t_start, t_end, max_steps);
+    if (b == 0 && threadIdx.x == 0) {
+        s.counters[0] = (int)gridDim.x < n_blocks ? (int)gridDim.x : n_blocks;
+        s.counters[1] = 0;
+    }
+}
+
+// One CTA per slot, after the sampler step of an iteration.
+__global__ void blocks_refill(const BlockSlots s, int L, int n_blocks, int32_t *block_tokens,
+                              int32_t *block_steps, int32_t *block_status, float t_start, float t_end,
+                              int max_steps)
+{
+    __shared__ int next;
+    const int b = blockIdx.x;
+    const int k = s.slot_block[b];
+    if (k < 0) return;                               // idle slot (CTA-uniform)
+    const int st = s.status[b];
+    if (st == EB_RUNNING) {
+        if (threadIdx.x == 0) {
+            const int step = s.slot_step[b] + 1;
+            s.slot_step[b] = step;
+            slot_temperature(t_start, t_end, max_steps, step, &s.slot_c[b], &s.slot_invT[b]);
+        }
+        return;
+    }
+    const long long base = (long long)b * L, out = (long long)k * L;
+    for (int p = threadIdx.x; p < L; p += blockDim.x) block_tokens[out + p] = s.tokens[base + p];
+    if (threadIdx.x == 0) {
+        if (block_steps) block_steps[k] = s.steps_taken[b];
+        if (block_status) block_status[k] = st;
+        atomicAdd(&s.counters[1], 1);
+        next = atomicAdd(&s.counters[0], 1);
+    }
+    __syncthreads();
+    slot_reset(s, b, L, next < n_blocks ? next : -1, t_start, t_end, max_steps);
+}
+
+struct BlocksLayout {
+    size_t step, mask, tokens, prev, status, steps, entropy, argmax, sampled, selected, block, sstep, c,
+        invT, counters, total;
+};
+
+BlocksLayout blocks_layout(int B, int L)
+{
+    const long long rows = (long long)B * L;
+    BlocksLayout o;
+    size_t at = 0;
+    auto take = [&](size_t bytes) { const size_t r = at; at += align256(bytes); return r; };
+    o.step = take(step_workspace_bytes(rows));
+    o.mask = take((size_t)rows);
+    o.tokens = take((size_t)rows * 4);
+    o.prev = take((size_t)rows * 4);
+    o.status = take((size_t)B * 4);
+    o.steps = take((size_t)B * 4);
+    o.entropy = take((size_t)rows * 4);
+    o.argmax = take((size_t)rows * 4);
+    o.sampled = take((size_t)rows * 4);
+    o.selected = take((size_t)rows);
+    o.block = take((size_t)B * 4);
+    o.sstep = take((size_t)B * 4);
+    o.c = take((size_t)B * 4);
+    o.invT = take((size_t)B * 4);
+    o.counters = take(16);
+    o.total = at;
+    return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t eb_blocks_workspace_bytes(int B, int L, int V, eb_dtype dtype)
+{
+    (void)V;
+    (void)dtype;
+    if (B < 1 || L < 1) return 0;
+    return blocks_layout(B, L).total;
+}
+
+eb_status eb_sample_blocks(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                           eb_block_logits_fn logits_fn, void *user, void *d_logits, int n_blocks,
+                           int32_t *d_block_tokens, int32_t *d_block_steps, int32_t *d_block_status,
+                           void *d_workspace, size_t workspace_bytes, int poll_every, int *iterations_run,
+                           void *stream)
+{
+    if (iterations_run) *iterations_run = 0;
+    if (!params) return fail(EB_ERR_INVALID, "params is NULL");
+    if (B < 1) return fail(EB_ERR_INVALID, "B must be >= 1 slot");
+    if (n_blocks < 0 || n_blocks > (1 << 24)) return fail(EB_ERR_INVALID, "n_blocks must be in [0, 2^24]");
+    if (!logits_fn) return fail(EB_ERR_INVALID, "logits_fn is NULL");
+    if (!d_block_tokens && n_blocks > 0) return fail(EB_ERR_INVALID, "d_block_tokens is NULL");
+    if (poll_every < 0) return fail(EB_ERR_INVALID, "poll_every must be >= 0");
+    const size_t need = eb_blocks_workspace_bytes(B, L, V, dtype);
+    char *ws = static_cast<char *>(d_workspace);
+    if (!ws || ((uintptr_t)ws & 255) != 0 || workspace_bytes < need)
+        return fail(EB_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+    const BlocksLayout o = blocks_layout(B, L);
+    BlockSlots sl;
+    sl.mask = reinterpret_cast<uint8_t *>(ws + o.mask);
+    sl.tokens = reinterpret_cast<int32_t *>(ws + o.tokens);
+    sl.prev_argmax = reinterpret_cast<int32_t *>(ws + o.prev);
+    sl.status = reinterpret_cast<int32_t *>(ws + o.status);
+    sl.steps_taken = reinterpret_cast<int32_t *>(ws + o.steps);
+    sl.entropy = reinterpret_cast<float *>(ws + o.entropy);
+    sl.argmax = reinterpret_cast<int32_t *>(ws + o.argmax);
+    sl.sampled = reinterpret_cast<int32_t *>(ws + o.sampled);
+    sl.selected = reinterpret_cast<uint8_t *>(ws + o.selected);
+    sl.slot_block = reinterpret_cast<int32_t *>(ws + o.block);
+    sl.slot_step = reinterpret_cast<int32_t *>(ws + o.sstep);
+    sl.slot_c = reinterpret_cast<float *>(ws + o.c);
+    sl.slot_invT = reinterpret_cast<float *>(ws + o.invT);
+    sl.counters = reinterpret_cast<int32_t *>(ws + o.counters);
+    StepBuffers sb{sl.mask, sl.tokens, sl.prev_argmax, sl.status, sl.steps_taken, sl.entropy, sl.argmax,
+                   sl.sampled, sl.selected, nullptr, nullptr, nullptr, nullptr};
+    sb.canvas_step = sl.slot_step;
+    sb.canvas_id = sl.slot_block;
+    sb.canvas_c = sl.slot_c;
+    sb.canvas_invT = sl.slot_invT;
+    eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, ws + o.step, o.mask - o.step,
+                                eb_workspace_bytes(B, L, V, dtype));
+    if (st != EB_OK) return st;
+    if (n_blocks == 0) return ok();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    blocks_init<<<B, 256, 0, s>>>(sl, L, n_blocks, params->t_start, params->t_end, params->max_steps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "block set-up launch: %s", cudaGetErrorString(e));
+    // every iteration advances every occupied slot by one step, so n_blocks * max_steps
+    // iterations finish any schedule; the host stops earlier once the finished count is n_blocks
+    const long long max_iter = (long long)n_blocks * params->max_steps;
+    int ran = 0;
+    for (long long it = 0; it < max_iter; ++it) {
+        if (poll_every > 0 && it > 0 && it % poll_every == 0) {
+            int32_t done = 0;
+            e = cudaMemcpyAsync(&done, sl.counters + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) {
+                if (iterations_run) *iterations_run = ran;
+                return fail(EB_ERR_CUDA, "progress read-back: %s", cudaGetErrorString(e));
+            }
+            if (done >= n_blocks) break;
+        }
+        if (logits_fn(user, B, sl.slot_block, sl.slot_step, sl.tokens, d_logits, stream) != 0) {
+            if (iterations_run) *iterations_run = ran;
+            return fail(EB_ERR_CALLBACK, "logits callback failed at iteration %lld", it);
+        }
+        st = launch_step(params, B, L, V, dtype, d_logits, 0, params->t_start, sb, ws + o.step, s);
+        if (st != EB_OK) {
+            if (iterations_run) *iterations_run = ran;
+            return st;
+        }
+        blocks_refill<<<B, 256, 0, s>>>(sl, L, n_blocks, d_block_tokens, d_block_steps, d_block_status,
+                                        params->t_start, params->t_end, params->max_steps);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            if (iterations_run) *iterations_run = ran;
+            return fail(EB_ERR_CUDA, "refill launch: %s", cudaGetErrorString(e));
+        }
+        ++ran;
+    }
+    if (iterations_run) *iterations_run = ran;
     return ok();
 }
 

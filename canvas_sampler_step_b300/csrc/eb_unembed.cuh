@@ -253,7 +253,7 @@ struct Tiles {
 // four groups of 8 through the streaming kernel's per-group body (each lane owns its row;
 // `gumbel` is off for lanes whose row is not masked).
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], int v0, bool on, bool gumbel, const Args &a,
-                                          uint32_t p, uint32_t sw, f32x2 c2, RowState &st, PackedSums &q,
+                                          const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
                                           float &nb, f32x2 &nb2, float &K, uint32_t stash)
 {
 #pragma unroll
@@ -262,7 +262,7 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], int v0, bool 
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[8 * g + j]);
         const int vg = v0 + 8 * g;
-        consume_vals<8, true, false>(x, on && vg < a.V, (uint32_t)vg, a, p, sw, c2, st, q, nb, nb2, K, gumbel,
+        consume_vals<8, true, false>(x, on && vg < a.V, (uint32_t)vg, a, rc, c2, st, q, nb, nb2, K, gumbel,
                                      stash);
     }
 }
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         f32x2 nb2 = 0ull;
         const f32x2 c2 = pk2(a.c, a.c);
         bool row_on = false, masked = false;
-        uint32_t p = 0, sw = 0;
+        RowCtx rc{a.c, a.invT, (uint32_t)a.step, 0u, 0u};
         for (; tl.valid();) {
             if (tl.mb != cur_mb) {
                 if (!LOGITS && cur_mb >= 0 && row_on) {
@@ -434,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int b = r / a.L;
                     row_on = a.status[b] == EB_RUNNING;
                     masked = a.mask[r] != 0;
-                    p = (uint32_t)(r - b * a.L);
-                    sw = (kStreamGumbel << 24) | (uint32_t)b;
+                    rc.p = (uint32_t)(r - b * a.L);
+                    rc.sw = (kStreamGumbel << 24) | (uint32_t)b;
                 }
                 st = empty_state();
                 packed_zero(qs);
@@ -461,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_ld32(base + (uint32_t)(32 * (ch + 1)), rb);
                     const int v0 = vbase + 32 * ch;
                     if (LOGITS) store_logits(ra, cur_mb * BM + rl, v0, a);
-                    else epi_chunk(ra, v0, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K, stash);
+                    else epi_chunk(ra, v0, row_on, masked, a, rc, c2, st, qs, nb, nb2, K, stash);
                     tc_wait32(rb);
                     if (ch + 2 < kEpiCols / 32) tc_ld32(base + (uint32_t)(32 * (ch + 2)), ra);
                     if (LOGITS) store_logits(rb, cur_mb * BM + rl, v0 + 32, a);
-                    else epi_chunk(rb, v0 + 32, row_on, masked, a, p, sw, c2, st, qs, nb, nb2, K, stash);
+                    else epi_chunk(rb, v0 + 32, row_on, masked, a, rc, c2, st, qs, nb, nb2, K, stash);
                     if (ch + 2 < kEpiCols / 32) tc_wait32(ra);
                 }
             }

@@ -119,16 +119,27 @@ __device__ __forceinline__ uint16_t to_bf16(float x)
 constexpr int kThreads = 256;
 constexpr int kGroupsPerThread = 8;
 
-// grid: x = chunks of kThreads * kGroupsPerThread groups of 4 entries, y = row (b * L + p)
+// grid: x = chunks of kThreads * kGroupsPerThread groups of 4 entries, y = row (b * L + p).
+// With slot_block, output canvas b is a slot that holds canvas slot_block[b] of the recipe
+// (skipped when negative) at step slot_step[b]; otherwise canvas b at `step`.
 __global__ void __launch_bounds__(kThreads) peaked_logits_kernel(const eb_synth_recipe r, int step,
-                                                                 const int32_t *status, void *out)
+                                                                 const int32_t *status,
+                                                                 const int32_t *slot_block,
+                                                                 const int32_t *slot_step, void *out)
 {
     __shared__ long long t_p;
     __shared__ float h_p;
     const long long row = blockIdx.y;
-    const int b = (int)(row / r.L);
-    const uint32_t p = (uint32_t)(row - (long long)b * r.L);
-    if (status && status[b] != 0) return;
+    const int ob = (int)(row / r.L);
+    const uint32_t p = (uint32_t)(row - (long long)ob * r.L);
+    int b = ob;
+    if (slot_block) {
+        b = slot_block[ob];
+        if (b < 0 || b >= r.B) return;
+        step = slot_step[ob];
+    } else if (status && status[b] != 0) {
+        return;
+    }
     const uint64_t seed = r.seed[b];
     if (threadIdx.x == 0) {
         const uint4 w = philox(make_uint4(0u, p, 0u, (kStreamPosition << 24) | (uint32_t)b), seed);
@@ -224,8 +235,32 @@ int eb_synth_logits(const eb_synth_recipe *r, int step, const int32_t *d_status,
     const long long per_cta = (long long)kThreads * kGroupsPerThread;
     dim3 grid((unsigned)((nk + per_cta - 1) / per_cta), (unsigned)(r->B * r->L));
     peaked_logits_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(*r, step, d_status,
-                                                                                  d_logits);
+                                                                                  nullptr, nullptr, d_logits);
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+int eb_synth_slot_logits(const eb_synth_recipe *r, int B_slots, const int32_t *d_slot_block,
+                         const int32_t *d_slot_step, void *d_logits, void *stream)
+{
+    if (!r || !d_logits || !d_slot_block || !d_slot_step || r->B < 1 || r->B > EB_SYNTH_MAX_B ||
+        r->L < 1 || r->V < 1 || (r->dtype != 0 && r->dtype != 1) || B_slots < 0 ||
+        (long long)B_slots * r->L > 65535)
+        return 1;
+    if (B_slots == 0) return 0;
+    const long long nk = ((long long)r->V + 3) / 4;
+    const long long per_cta = (long long)kThreads * kGroupsPerThread;
+    dim3 grid((unsigned)((nk + per_cta - 1) / per_cta), (unsigned)(B_slots * r->L));
+    peaked_logits_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(*r, 0, nullptr, d_slot_block,
+                                                                                  d_slot_step, d_logits);
+    return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+int eb_synth_block_callback(void *user, int B, const int32_t *d_slot_block, const int32_t *d_slot_step,
+                            const int32_t *d_tokens, void *d_logits, void *stream)
+{
+    (void)d_tokens;
+    return eb_synth_slot_logits(static_cast<const eb_synth_recipe *>(user), B, d_slot_block, d_slot_step,
+                                d_logits, stream);
 }
 
 int eb_synth_logits_callback(void *user, int step, const int32_t *d_tokens, const int32_t *d_status,

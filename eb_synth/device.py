@@ -14,7 +14,8 @@ SRC = os.path.join(_HERE, "csrc", "eb_synth.cu")
 HDR = os.path.join(_ROOT, "include", "eb_synth.h")
 LIB_PATH = os.path.join(_HERE, "libeb_synth.so")
 MAX_B = 64
-EXPORTED = ("eb_synth_logits", "eb_synth_logits_callback", "eb_synth_unembed_inputs")
+EXPORTED = ("eb_synth_logits", "eb_synth_logits_callback", "eb_synth_unembed_inputs",
+            "eb_synth_slot_logits", "eb_synth_block_callback")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -61,6 +62,10 @@ def lib() -> ctypes.CDLL:
         L.eb_synth_unembed_inputs.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, ctypes.c_float, ctypes.c_float, P, P, P]
         L.eb_synth_unembed_inputs.restype = ctypes.c_int
+        L.eb_synth_slot_logits.argtypes = [ctypes.POINTER(Recipe), ctypes.c_int, P, P, P, P]
+        L.eb_synth_slot_logits.restype = ctypes.c_int
+        L.eb_synth_block_callback.argtypes = [P, ctypes.c_int, P, P, P, P, P]
+        L.eb_synth_block_callback.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -92,3 +97,16 @@ def unembed_inputs(seed: int, M: int, K: int, V: int, sigma_w: float, bias: floa
                                        _stream(stream))
     if rc != 0:
         raise RuntimeError(f"eb_synth_unembed_inputs failed ({rc})")
+
+
+def slot_logits(recipe: Recipe, slot_block, slot_step, out, stream=None) -> None:
+    """Fill slot b of ``out`` [B_slots, L, V] with recipe canvas slot_block[b] at slot_step[b]."""
+    rc = lib().eb_synth_slot_logits(ctypes.byref(recipe), int(slot_block.numel()), slot_block.data_ptr(),
+                                    slot_step.data_ptr(), out.data_ptr(), _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"eb_synth_slot_logits failed ({rc})")
+
+
+def block_callback_address() -> int:
+    """Address of eb_synth_block_callback (an eb_block_logits_fn; user = Recipe*)."""
+    return ctypes.cast(lib().eb_synth_block_callback, ctypes.c_void_p).value

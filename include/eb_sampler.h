@@ -65,6 +65,7 @@ typedef enum { EB_F32 = 0, EB_BF16 = 1 } eb_dtype;
 #define EB_STOP_CAP 3            /* the last step (max_steps - 1) was reached */
 #define EB_STATUS_NONFINITE 0x100 /* or-ed in: NaN / +-Inf logits seen; canvas halted */
 #define EB_STATUS_TIMEOUT 0x200   /* or-ed in: a bounded device wait gave up; canvas halted */
+#define EB_SLOT_IDLE 0x400        /* eb_sample_blocks: a slot holding no block */
 
 typedef struct {
     int32_t max_steps;     /* 48 */
@@ -209,6 +210,54 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
                            float *d_entropy, int32_t *d_argmax, int32_t *d_sampled,
                            uint8_t *d_selected, void *d_workspace, size_t workspace_bytes,
                            int poll_every, int *steps_run, void *stream);
+
+/* Denoiser of the block driver: enqueue, on `stream`, the logits of every occupied slot b
+ * (d_slot_block[b] >= 0: the block it holds) at that block's own step d_slot_step[b] into
+ * d_logits [B, L, V]; slots with d_slot_block[b] < 0 are idle and may be left as they are.
+ * d_tokens [B, L] holds each slot's canvas (committed tokens, -1 where masked).  All four
+ * arrays are device memory.  Returns 0 on success. */
+typedef int (*eb_block_logits_fn)(void *user, int B, const int32_t *d_slot_block,
+                                  const int32_t *d_slot_step, const int32_t *d_tokens,
+                                  void *d_logits, void *stream);
+
+/* Bytes of device workspace eb_sample_blocks needs for B slots of L positions: the step
+ * workspace plus the slots' canvas state.  256-byte aligned; no initialisation needed. */
+size_t eb_blocks_workspace_bytes(int B, int L, int V, eb_dtype dtype);
+
+/*
+ * Block driver with continuous batching.  DiffusionGemma generates block-autoregressively:
+ * a canvas is denoised until done, then the model moves on to the next canvas (model card,
+ * "Model overview", multi-canvas sampling), and each canvas stops on its own step count
+ * ("Best practices" section 1, adaptive stop).  The pages give no serving loop; this is the
+ * plainest one that keeps every slot busy.  n_blocks canvases
+ * ("blocks") of L positions are generated on B slots.  Block k starts all masked at step 0,
+ * with k as its canvas id in the Gumbel noise's Philox counter (so its result does not depend
+ * on the slot it runs in), and follows the denoising loop of eb_sample_canvas: each
+ * iteration, logits_fn fills the occupied slots' logits, one sampler step runs with every
+ * slot at its block's own step and schedule temperature, and a slot whose block stopped
+ * writes the block's tokens, step count and stop reason and takes the next block, or goes
+ * idle (EB_SLOT_IDLE) when none is left.  Blocks are handed to slots in the order the slots
+ * free up, which the results do not depend on.
+ *
+ *   params            as in eb_sampler_step (flags included)
+ *   B                 slots (>= 1); L, V, dtype as in eb_sampler_step
+ *   logits_fn, user   the denoiser (above); d_logits its [B, L, V] output buffer
+ *   n_blocks          blocks to generate (0 .. 2^24)
+ *   d_block_tokens    [n_blocks, L] i32 out: each block's final tokens
+ *   d_block_steps     [n_blocks] i32 out or NULL: steps the block ran
+ *   d_block_status    [n_blocks] i32 out or NULL: its stop reason (EB_STOP_* plus status bits)
+ *   d_workspace       eb_blocks_workspace_bytes(B, L, V, dtype) bytes, 256-byte aligned
+ *   poll_every        read the finished-block count back every `poll_every` iterations and
+ *                     stop once all are done (0: run the bound of n_blocks * max_steps
+ *                     iterations, the idle ones costing no sampler work)
+ *   iterations_run    host out (may be NULL): iterations enqueued
+ * Returns EB_ERR_CALLBACK (after enqueuing nothing further) if logits_fn fails.
+ */
+eb_status eb_sample_blocks(const eb_params *params, int B, int L, int V, eb_dtype dtype,
+                           eb_block_logits_fn logits_fn, void *user, void *d_logits, int n_blocks,
+                           int32_t *d_block_tokens, int32_t *d_block_steps, int32_t *d_block_status,
+                           void *d_workspace, size_t workspace_bytes, int poll_every,
+                           int *iterations_run, void *stream);
 
 /*
  * Fused unembedding + sampler step.  The logits of the step are the product of the decoder's

@@ -44,6 +44,16 @@ int eb_synth_logits(const eb_synth_recipe *recipe, int step, const int32_t *d_st
 int eb_synth_logits_callback(void *user, int step, const int32_t *d_tokens,
                              const int32_t *d_status, void *d_logits, void *stream);
 
+/* Denoiser of the block driver: slot b of d_logits [B_slots, L, V] receives the logits of
+ * recipe canvas k = d_slot_block[b] (0 <= k < recipe->B; other slots are left as they are) at
+ * step d_slot_step[b], exactly as eb_synth_logits writes canvas k at that step. */
+int eb_synth_slot_logits(const eb_synth_recipe *recipe, int B_slots, const int32_t *d_slot_block,
+                         const int32_t *d_slot_step, void *d_logits, void *stream);
+
+/* Same signature as eb_block_logits_fn of eb_sampler.h: user = const eb_synth_recipe* (host). */
+int eb_synth_block_callback(void *user, int B, const int32_t *d_slot_block, const int32_t *d_slot_step,
+                            const int32_t *d_tokens, void *d_logits, void *stream);
+
 /* Fused-unembedding inputs: h [M, K] = N(0,1) and W [K, V] = sigma_w * N(0,1) plus `bias`
  * at column c_k = (w0 * V) >> 32 of each row k (counter (0, k, 0, 6 << 24)), as bfloat16.
  * h uses counter (j / 4, m, 0, 5 << 24) over its K columns j; W uses (v / 4, k, 0, 7 << 24). */

@@ -18,6 +18,7 @@ step(...)                  -- one full sampler step over B canvases (stats, stop
 unembed_logits(h, W)       -- the decoder's unembedding product h W in binary64 (the logits
                               the fused path feeds to the sampler without storing them)
 run_loop(...)              -- the <= 48-step denoising loop with per-canvas stop
+run_blocks(...)            -- the block driver's result: every block through its own loop
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py`` except the
 readings the pages leave open (shaped-entropy stop statistic, mean over all positions,
@@ -79,7 +80,7 @@ def _load():
     lib.eb_oracle_select.restype = ctypes.c_int
     lib.eb_oracle_step.argtypes = [ctypes.c_int, ctypes.c_int, i64, ctypes.c_int, P,
                                    ctypes.c_int, f64, ctypes.c_int, f64, f64, f64, f64, u64,
-                                   ctypes.c_uint32,
+                                   ctypes.c_uint32, P,
                                    P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.eb_oracle_step.restype = None
     lib.eb_oracle_num_threads.argtypes = []
@@ -219,8 +220,9 @@ class StepResult:
 
 
 def step(logits: np.ndarray, state: State, step_index: int, params: Params = Params(),
-         temperature: float = 0.0) -> StepResult:
-    """One EB sampler step over logits [B, L, V]; updates ``state`` in place."""
+         temperature: float = 0.0, canvas_ids=None) -> StepResult:
+    """One EB sampler step over logits [B, L, V]; updates ``state`` in place.  ``canvas_ids``
+    ([B] ints, default 0..B-1) are the canvases' ids in the Gumbel noise's Philox counter."""
     x, dt = _logits_array(logits)
     B, L, V = x.shape
     st = state
@@ -238,9 +240,13 @@ def step(logits: np.ndarray, state: State, step_index: int, params: Params = Par
     sm = np.zeros(B, np.float64)
     om = np.zeros(B, np.float64)
     stm = np.zeros(B, np.float64)
+    ids = None if canvas_ids is None else np.ascontiguousarray(canvas_ids, np.int32)
+    if ids is not None and ids.shape != (B,):
+        raise ValueError("canvas_ids must have one entry per canvas")
     _load().eb_oracle_step(B, L, V, dt, _ptr(x), int(step_index), float(temperature),
                            params.max_steps, params.t_start, params.t_end, params.entropy_bound,
                            params.stop_entropy, params.seed, params.flags,
+                           _ptr(ids) if ids is not None else None,
                            _ptr(st.mask), _ptr(st.tokens), _ptr(st.prev_argmax), _ptr(st.status),
                            _ptr(st.steps_taken), _ptr(H), _ptr(A), _ptr(Y), _ptr(gap), _ptr(sel),
                            _ptr(committed), _ptr(meanH), _ptr(sm), _ptr(om), _ptr(stm))
@@ -250,7 +256,7 @@ def step(logits: np.ndarray, state: State, step_index: int, params: Params = Par
 
 
 def run_loop(logits_fn, B: int, L: int, params: Params = Params(), state: State | None = None,
-             start_step: int = 0, on_step=None) -> State:
+             start_step: int = 0, on_step=None, canvas_ids=None) -> State:
     """The denoising loop: for s in [start_step, max_steps) while any canvas runs,
     logits_fn(s, state) -> [B, L, V] logits, then one sampler step.  ``on_step(s, result,
     state)`` sees every step's result (for lockstep comparison)."""
@@ -258,10 +264,25 @@ def run_loop(logits_fn, B: int, L: int, params: Params = Params(), state: State 
     for s in range(start_step, params.max_steps):
         if not np.any(st.status == RUNNING):
             break
-        res = step(logits_fn(s, st), st, s, params)
+        res = step(logits_fn(s, st), st, s, params, canvas_ids=canvas_ids)
         if on_step is not None:
             on_step(s, res, st)
     return st
+
+
+def run_blocks(block_logits_fn, n_blocks: int, L: int, params: Params = Params()):
+    """What the block driver computes, block by block: block k is a fresh all-masked canvas of L
+    positions, with k as its Philox canvas id, run through the denoising loop on its own
+    (block_logits_fn(k, s) -> [L, V] logits of block k at its step s).  The slots and the order
+    in which they take blocks do not enter.  Returns (tokens [n, L], steps [n], status [n])."""
+    tokens = np.zeros((n_blocks, L), np.int32)
+    steps = np.zeros(n_blocks, np.int32)
+    status = np.zeros(n_blocks, np.int32)
+    for k in range(n_blocks):
+        st = run_loop(lambda s, _st, k=k: block_logits_fn(k, s)[None], 1, L, params,
+                      canvas_ids=[k])
+        tokens[k], steps[k], status[k] = st.tokens[0], st.steps_taken[0], st.status[0]
+    return tokens, steps, status
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:

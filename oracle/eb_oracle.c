@@ -268,11 +268,13 @@ int eb_oracle_select(int L, const double *H, const uint8_t *mask, double bound,
  * Order within a step: row statistics -> stop test (s >= 1) -> on stop, every masked
  * position takes its argmax; otherwise selection and commit of the sampled tokens, then
  * the complete / cap check (at the cap the rest take their argmax) -> prev_argmax = A.
- * temperature <= 0 selects the linear schedule; flags selects the reading variants above. */
+ * temperature <= 0 selects the linear schedule; flags selects the reading variants above;
+ * canvas_ids (NULL: b) gives each canvas's id in the Gumbel noise's Philox counter, which the
+ * block driver sets to the block number. */
 void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
                     int step, double temperature,
                     int max_steps, double t_start, double t_end, double bound,
-                    double stop_entropy, uint64_t seed, uint32_t flags,
+                    double stop_entropy, uint64_t seed, uint32_t flags, const int32_t *canvas_ids,
                     uint8_t *mask, int32_t *tokens, int32_t *prev_argmax,
                     int32_t *status, int32_t *steps_taken,
                     double *H, int32_t *A, int32_t *Y, double *gap, uint8_t *selected,
@@ -293,7 +295,8 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
             continue;
         }
         const char *row = (const char *)logits + (size_t)r * (size_t)V * esize;
-        eb_oracle_row(row, dtype, V, T, mask[r], seed, b, p, step, &H[r], &A[r], &Y[r], &gap[r]);
+        eb_oracle_row(row, dtype, V, T, mask[r], seed, canvas_ids ? canvas_ids[b] : b, p, step,
+                      &H[r], &A[r], &Y[r], &gap[r]);
     }
 
     for (int b = 0; b < B; ++b) {

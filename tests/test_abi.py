@@ -116,3 +116,27 @@ def test_loop_rejects_missing_callback(libs):
 def test_status_strings(libs):
     for s in range(6):
         assert eb.lib().eb_status_string(s)
+
+
+def test_block_driver_rejects_bad_arguments(libs):
+    p = eb.eb_default_params()
+    ws = eb.eb_blocks_workspace_bytes(2, 32, 64, eb.EB_F32)
+    assert ws > eb.eb_workspace_bytes(2, 32, 64, eb.EB_F32) and ws % 256 == 0
+    assert eb.eb_blocks_workspace_bytes(0, 32, 64, eb.EB_F32) == 0
+    cases = [
+        (dict(B=0), eb.EB_ERR_INVALID),
+        (dict(n_blocks=-1), eb.EB_ERR_INVALID),
+        (dict(logits_fn=0), eb.EB_ERR_INVALID),
+        (dict(block_tokens=None), eb.EB_ERR_INVALID),
+        (dict(workspace_bytes=16), eb.EB_ERR_WORKSPACE),
+        (dict(workspace=FAKE + 8), eb.EB_ERR_WORKSPACE),
+        (dict(L=1025, workspace_bytes=1 << 40), eb.EB_ERR_INVALID),
+    ]
+    for kw, status in cases:
+        args = dict(params=p, B=2, L=32, V=64, dtype=eb.EB_F32, logits_fn=FAKE, user=None, logits=FAKE,
+                    n_blocks=3, block_tokens=FAKE, block_steps=None, block_status=None,
+                    workspace=FAKE, workspace_bytes=ws, poll_every=0, stream=0)
+        args.update(kw)
+        with pytest.raises(eb.EbError) as ei:
+            eb.eb_sample_blocks(**args)
+        assert ei.value.status == status, kw

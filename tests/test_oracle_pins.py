@@ -418,3 +418,24 @@ def test_finalize_sampled_takes_the_sampled_token_at_stop_and_cap():
         assert fin.sum() == L - 2
         assert (st.tokens[0][fin] == getattr(r, key)[0][fin]).all()
         assert (r.Y[0][fin] != r.A[0][fin]).sum() >= 3
+
+
+# ---------------------------------------------------------------- block driver
+
+def test_blocks_run_alone_equal_the_batch_loop():
+    """Block k run on its own with Philox canvas id k reproduces canvas k of the loop over all
+    blocks at once, and the id is what makes it so: the same block under id 0 samples
+    differently."""
+    import eb_synth
+    cfg = eb_synth.Peaked(3, 16, 256, "f32", 3.0, 0.0, 4.0, (0.4, 0.8, 0.2), (7, 8, 9))
+    op = oracle.Params(seed=2)
+    st = oracle.run_loop(lambda s, _st: cfg.logits(s), 3, 16, op)
+    tok, steps, status = oracle.run_blocks(lambda k, s: cfg.logits(s)[k], 3, 16, op)
+    assert np.array_equal(tok, st.tokens)
+    assert np.array_equal(steps, st.steps_taken) and np.array_equal(status, st.status)
+    x = cfg.logits(0)[1:2]
+    r_own = oracle.step(x, oracle.State.fresh(1, 16), 0, op, canvas_ids=[1])
+    r_zero = oracle.step(x, oracle.State.fresh(1, 16), 0, op, canvas_ids=[0])
+    r_batch = oracle.step(cfg.logits(0)[:2], oracle.State.fresh(2, 16), 0, op)
+    assert np.array_equal(r_own.Y[0], r_batch.Y[1])
+    assert (r_own.Y[0] != r_zero.Y[0]).sum() >= 4

@@ -432,7 +432,7 @@ struct RowCtx {
 };
 
 // N = 8 or 4 consecutive logits x of a canvas row, entries v0 .. v0+N-1 (v0 a multiple of
-// N): running max / first argmax, S and T2 (on packed f32x2 pairs when EB_PACKED is 1), and
+// N): running max / first argmax, S and T2 (on packed f32x2 pairs), and
 // for masked rows the per-entry Gumbel candidate test 1 - u < 2^t K, whose rare passes take
 // the exact score.  `a` supplies c = log2(e)/T, invT = 1/T, the step and the Philox round
 // keys.  WARP_ROW: the 32 lanes work on the same row (they share the best score when it
@@ -441,9 +441,6 @@ struct RowCtx {
 // off for a lane whose row is not masked.  `stash` (per-thread rows only) is the shared address
 // of a 32-byte slot of this thread that keeps a candidate group's Philox words for the exact
 // pass; with WARP_ROW the pass draws them again.
-#ifndef EB_PACKED
-#define EB_PACKED 1
-#endif
 template <int N, bool MASKED, bool WARP_ROW, typename Args>
 __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, uint32_t v0, const Args &a,
                                              const RowCtx &rc, f32x2 c2, RowState &st,
@@ -501,7 +498,6 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
         }
     }
     if (valid) {
-#if EB_PACKED
 #pragma unroll
         for (int i = 0; i < N / 2; ++i) {
             const f32x2 tp = fma2(pk2(x[2 * i], x[2 * i + 1]), c2, nb2);
@@ -518,25 +514,6 @@ __device__ __forceinline__ void consume_vals(const float (&x)[N], bool valid, ui
                 q.T0 = fma2(tp, ep, q.T0);
             }
         }
-#else
-        // scalar accumulation into the four lanes of the packed sums (S0.lo, S0.hi, S1.lo, S1.hi)
-        float s[4], t2[4];
-        upk2(q.S0, s[0], s[1]);
-        upk2(q.S1, s[2], s[3]);
-        upk2(q.T0, t2[0], t2[1]);
-        upk2(q.T1, t2[2], t2[3]);
-#pragma unroll
-        for (int j = 0; j < N; ++j) {
-            const float t = fmaf(x[j], rc.c, nb);
-            e[j] = ex2(t);
-            s[j & 3] += e[j];
-            t2[j & 3] = fmaf(t, e[j], t2[j & 3]);
-        }
-        q.S0 = pk2(s[0], s[1]);
-        q.S1 = pk2(s[2], s[3]);
-        q.T0 = pk2(t2[0], t2[1]);
-        q.T1 = pk2(t2[2], t2[3]);
-#endif
     }
     if constexpr (MASKED) {
         bool cand = false;

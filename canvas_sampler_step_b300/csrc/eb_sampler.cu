@@ -237,16 +237,18 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, f
     consumer_sync();
 }
 
-// ------------------------------------------------------------------ direct-load path
+// ------------------------------------------------------------------ streaming path
 //
-// The same row statistics without the shared-memory ring: every warp is one unit of the
-// weighted partition (its slot is row + global warp index) and streams its row segments with
-// 16-byte loads that bypass L1, U vectors per lane per batch, the next batch in flight while
-// the current one is consumed.  Warps merge their lanes with shuffles; no block barrier runs
-// after the prefix is built.
+// Every warp is one unit of the weighted partition (its slot is row + global warp index) and
+// streams its row segments: each lane stages its own 16-byte vectors in shared memory with
+// cp.async, kAsyncDepth batches of U vectors ahead, so that no barrier is shared between
+// lanes.  Warps merge their lanes with shuffles; no block barrier runs after the prefix is
+// built.
 constexpr int kDirectThreads = 512;
 constexpr int kDirectWarps = kDirectThreads / 32;
 constexpr int kDirectU = 2;             // vectors per lane per batch
+constexpr int kAsyncDepth = 4;          // batches in flight per lane
+constexpr int kDirectStageBytes = kAsyncDepth * kDirectU * kDirectThreads * 16;
 
 // L2 policy for the logits: evicted first, so that streaming them does not push out the
 // workspace (partials, row units) that the selection kernel reads right after.
@@ -257,6 +259,7 @@ __device__ __forceinline__ uint64_t evict_first_policy()
     return pol;
 }
 
+// Plain 16-byte load of the ragged tail of a segment (bypassing L1, evict-first in L2).
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 {
     uint4 r;
@@ -265,70 +268,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
                  : "l"(p), "l"(evict_first_policy()));
     return r;
 }
-
-template <int U>
-__device__ __forceinline__ void load_full(uint4 (&r)[U], const uint4 *src, uint32_t jb, uint32_t lane)
-{
-#pragma unroll
-    for (int u = 0; u < U; ++u) r[u] = ld_stream(src + jb + lane + 32u * (uint32_t)u);
-}
-
-template <int VEC, int U>
-__device__ __forceinline__ void consume_full(const uint4 (&r)[U], uint32_t jb, uint32_t lane, const K1Args &a,
-                                             const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
-                                             float &nb, f32x2 &nb2, float &K, bool gumbel)
-{
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-        consume_packed<VEC, true>(r[u], true, jb + lane + 32u * (uint32_t)u, a, rc, c2, st, q, nb, nb2, K,
-                                  gumbel);
-}
-
-// One row segment [j0, j1) of a warp: whole batches of 32 U vectors run without bounds
-// checks from two register buffers (the next batch loads while the current one is consumed),
-// the remainder with checks.
-// One code instance serves masked and unmasked rows (`gumbel` is warp-uniform), which keeps
-// the unrolled loop small enough for the instruction cache.
-template <int VEC, int U>
-__device__ __forceinline__ void direct_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
-                                               const RowCtx &rc, f32x2 c2, RowState &st,
-                                               PackedSums &q, bool gumbel)
-{
-    constexpr uint32_t kBatch = 32u * U;
-    const uint32_t lane = threadIdx.x & 31;
-    float nb = -st.xm * rc.c;
-    f32x2 nb2 = pk2(nb, nb);
-    float K = cand_scale(st.xm, st.best, rc.c);
-    const uint32_t jf = j0 + (j1 - j0) / kBatch * kBatch;
-    if (jf > j0) {
-        uint4 A[U], B[U];
-        load_full<U>(A, src, j0, lane);
-        for (uint32_t jb = j0;; jb += 2 * kBatch) {
-            const bool hasB = jb + kBatch < jf;
-            if (hasB) load_full<U>(B, src, jb + kBatch, lane);
-            consume_full<VEC, U>(A, jb, lane, a, rc, c2, st, q, nb, nb2, K, gumbel);
-            if (!hasB) break;
-            const bool hasA = jb + 2 * kBatch < jf;
-            if (hasA) load_full<U>(A, src, jb + 2 * kBatch, lane);
-            consume_full<VEC, U>(B, jb + kBatch, lane, a, rc, c2, st, q, nb, nb2, K, gumbel);
-            if (!hasA) break;
-        }
-    }
-#pragma unroll 1
-    for (uint32_t jb = jf; jb < j1; jb += 32u) {
-        const uint32_t idx = jb + lane;
-        const bool valid = idx < j1;
-        const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-        consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
-    }
-}
-
-// --- the same segment through per-lane cp.async staging (async_segment below)
-#ifndef EB_ASYNC_DEPTH
-#define EB_ASYNC_DEPTH 4
-#endif
-constexpr int kAsyncDepth = EB_ASYNC_DEPTH;
-constexpr int kDirectStageBytes = kAsyncDepth * kDirectU * kDirectThreads * 16;
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -467,8 +406,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
         RowState st = empty_state();
         PackedSums q;
         packed_zero(q);
-        if (kAsyncDepth > 0) async_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, rc, c2, st, q, masked, stage);
-        else direct_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, rc, c2, st, q, masked);
+        async_segment<VEC, U>(a, src, (uint32_t)j0, (uint32_t)j1, rc, c2, st, q, masked, stage);
         packed_fold(q, st);
         const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
         warp_merge(st, rc.c);
@@ -1037,7 +975,6 @@ float schedule_temperature(const eb_params *p, int step)
     return p->t_start + (p->t_end - p->t_start) * (float)step / (float)(p->max_steps - 1);
 }
 
-// Workspace layout: [partials (rows + kMaxGrid) x 32 B][weight prefix (rows + 1) x 4 B].
 // Workspace layout: [partials (rows + kMaxGrid) x 32 B][weight prefix (rows + 1) x 4 B]
 // [first / last partition unit of each row, rows x 8 B], each part 256-byte aligned.
 constexpr size_t align256c(size_t x) { return (x + 255) & ~(size_t)255; }

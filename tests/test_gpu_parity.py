@@ -233,6 +233,26 @@ def test_step_parity_longest_canvas():
     assert res.committed[0] > 32
 
 
+def test_step_parity_beyond_the_weighted_partition():
+    """B*L = 17 x 256 = 4352 rows exceed the weighted partition's 4096-row limit, so the
+    closed-form uniform partition runs instead; it skips a halted canvas by its status."""
+    cfg = eb_synth.Peaked(17, 256, 1024, "f32", 3.0, 0.0, 4.0, (0.0,) * 17, tuple(range(17)))
+    rng = np.random.default_rng(3)
+    mask = (rng.random((17, 256)) < 0.5).astype(np.uint8)
+    mask[:, 0] = 1
+
+    def halt(c, ost):
+        c.status[5] = eb.EB_STOP_CAP
+        ost.status[5] = oracle.CAP
+
+    g, res, ost, running = _run_step(cfg, 0, mask=mask, state=halt)
+    assert not running[5]
+    rep = Report()
+    compare_step(g, res, ost, running, rep, ctx="uniform partition")
+    assert rep.canvases == 16 and rep.canvas_ties <= 4
+    assert g["status"][5] == eb.EB_STOP_CAP and np.array_equal(g["mask"][5], mask[5])
+
+
 def _check_selection_properties(g, mask_before, bound=np.float32(0.1)):
     """Selection validity from the GPU's own entropies: the committed masked positions
     are the k lowest (H, p) and k follows the prefix rule (up to the tie window)."""

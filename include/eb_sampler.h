@@ -21,7 +21,9 @@
  *      masked take A (step cap).
  * The pages give no selection formula; the rule of item 4 is the one this library
  * implements (the longest sorted prefix whose sum minus its maximum stays within the
- * bound).
+ * bound).  Items 3 and 5 state the default readings of two open points; EB_FLAG_* bits of
+ * eb_params.flags select the alternatives (stop statistics over the masked positions only,
+ * sampled-token finalisation).
  *
  * Conventions shared by every entry point:
  *   - every d_* pointer is DEVICE memory owned by the caller; the library allocates

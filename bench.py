@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--logits", choices=("bf16", "fp8"), default="bf16",
+                    help="element type of the single-step workload's logits (fp8: OCP e4m3)")
     ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "blocks"), default="single",
                     help="single: the single-step workload (default, the headline line); fused: "
                          "the fused unembedding + sampler step (4 x 256 positions, K=2048); "
@@ -227,6 +229,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the workload
 
+def logits_kind(args, eb, torch):
+    """Element type of the single-step workload: bf16 (the headline) or OCP e4m3."""
+    import dataclasses
+
+    import eb_synth
+    if getattr(args, "logits", "bf16") == "fp8":
+        return {"name": "e4m3", "torch": torch.uint8, "eb": eb.EB_FP8_E4M3, "bytes": B * L * V,
+                "cfg": lambda seed: dataclasses.replace(eb_synth.cfg1(seed), dtype="fp8"),
+                "metric": METRIC.replace("bf16", "e4m3"),
+                "workload": WORKLOAD.replace("bf16 logits", "e4m3 logits (the bf16 workload's values "
+                                             "rounded to e4m3)")}
+    return {"name": "bf16", "torch": torch.int16, "eb": eb.EB_BF16, "bytes": BYTES_PER_STEP,
+            "cfg": eb_synth.cfg1, "metric": METRIC, "workload": WORKLOAD}
+
+
 def workload_masks():
     import eb_synth
     return np.stack([eb_synth.cfg1_mask(seed)[0] for seed in range(NSEEDS)])
@@ -285,10 +302,11 @@ def run_ours(args, rank, world, local):
     sp = stream.cuda_stream
 
     # inputs resident in HBM before the timed region
+    lk = logits_kind(args, eb, torch)
     bufs = []
     for seed in range(NSEEDS):
-        x = torch.empty((B, L, V), dtype=torch.int16, device=device)
-        synth_dev.logits(synth_dev.Recipe.of(eb_synth.cfg1(seed)), 0, x)
+        x = torch.empty((B, L, V), dtype=lk["torch"], device=device)
+        synth_dev.logits(synth_dev.Recipe.of(lk["cfg"](seed)), 0, x)
         bufs.append(x)
     masks = workload_masks()
     K, W = args.steps, args.warmup
@@ -302,7 +320,7 @@ def run_ours(args, rank, world, local):
     ptrs = [state_ptrs(pool, i) for i in range(N)]
     wpool = state_pool(W, masks, device)
     wptrs = [state_ptrs(wpool, i) for i in range(W)]
-    ws_bytes = eb.eb_workspace_bytes(B, L, V, eb.EB_BF16)
+    ws_bytes = eb.eb_workspace_bytes(B, L, V, lk["eb"])
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     params = eb.eb_default_params(seed=0)
     pref = ctypes.byref(params)
@@ -311,7 +329,7 @@ def run_ours(args, rank, world, local):
     step_fn = lib.eb_sampler_step
 
     def one(i, sptrs, stream_ptr):
-        st = step_fn(pref, B, L, V, eb.EB_BF16, buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *sptrs[i],
+        st = step_fn(pref, B, L, V, lk["eb"], buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *sptrs[i],
                      wsp, ws_bytes, stream_ptr)
         if st != 0:
             raise eb.EbError(st, lib.eb_last_error().decode())
@@ -372,13 +390,13 @@ def run_ours(args, rank, world, local):
 
     k1_avg_s = statistics.mean(k1_ms) / 1e3
     peak, peak_kind = measured_peaks()
-    achieved = BYTES_PER_STEP / k1_avg_s / 1e9
-    traffic = recorded_traffic()
+    achieved = lk["bytes"] / k1_avg_s / 1e9
+    traffic = recorded_traffic() if lk["name"] == "bf16" else None
 
-    e2e = run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world)
+    e2e = run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world, lk)
 
     out = {
-        "metric": METRIC,
+        "metric": lk["metric"],
         "value": value,
         "unit": "steps/s",
         "n_gpus": world,
@@ -391,18 +409,18 @@ def run_ours(args, rank, world, local):
         "dtype": "f32",
         "data": "synthetic (seeded Philox / Box-Muller logits, eb_synth)",
         "config": {
-            "workload": WORKLOAD,
-            "B": B, "L": L, "V": V, "logits_dtype": "bf16", "masked": 128, "temperature": TEMPERATURE,
-            "l2": "10 rotating 128 MiB logit buffers (1.25 GiB > 126 MB L2)",
+            "workload": lk["workload"],
+            "B": B, "L": L, "V": V, "logits_dtype": lk["name"], "masked": 128, "temperature": TEMPERATURE,
+            "l2": f"10 rotating {lk['bytes'] >> 20} MiB logit buffers ({10 * lk['bytes'] / 2**30:.3g} GiB > 126 MB L2)",
             "launch": f"CUDA graph of {N} steps (+ one canvas-state restore) replayed {R} times; "
                       f"row-statistics kernel timed by events on {len(prof_steps)} steps per replay",
             "parallelism": f"replicas x{world}",
         },
-        "hbm_gbs_step": BYTES_PER_STEP * K / elapsed / 1e9,
+        "hbm_gbs_step": lk["bytes"] * K / elapsed / 1e9,
         "positions_per_s": value * B * L,
         "roofline": {
             "bound": "hbm",
-            "kernel": "k1_rowstats<bf16>",
+            "kernel": f"k1_rowstats<{lk['name']}>",
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
@@ -411,7 +429,7 @@ def run_ours(args, rank, world, local):
             "traffic": traffic,
             "k1_ms_mean": statistics.mean(k1_ms),
             "k1_ms_median": statistics.median(k1_ms),
-            "bytes_per_launch": BYTES_PER_STEP,
+            "bytes_per_launch": lk["bytes"],
         },
         "e2e": e2e,
         "gpu_launches": 2 * K,                 # row statistics + selection per step
@@ -425,7 +443,7 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
-def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world):
+def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world, lk):
     """Same steps through the C ABI with host buffers: per step the pinned-host logits
     and canvas state go to the device, the step runs, its results come back."""
     import ctypes
@@ -441,11 +459,11 @@ def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, wor
     ptrs = state_ptrs(dstate, 0)
     out_keys = ("tokens", "mask", "status", "entropy", "argmax", "sampled", "selected")
     hout = {k: torch.empty_like(dstate[k], device="cpu").pin_memory() for k in out_keys}
-    ws_bytes = eb.eb_workspace_bytes(B, L, V, eb.EB_BF16)
+    ws_bytes = eb.eb_workspace_bytes(B, L, V, lk["eb"])
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     pref = ctypes.byref(params)
     sp = stream.cuda_stream
-    h2d = host_logits[0].numel() * 2 + sum(
+    h2d = host_logits[0].numel() * host_logits[0].element_size() + sum(
         hstate[0][k].numel() * hstate[0][k].element_size() for k in in_keys)
     d2h = sum(hout[k].numel() * hout[k].element_size() for k in out_keys)
 
@@ -454,7 +472,7 @@ def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, wor
         dev_logits.copy_(host_logits[s], non_blocking=True)
         for k in in_keys:
             dstate[k].copy_(hstate[s][k], non_blocking=True)
-        st = lib.eb_sampler_step(pref, B, L, V, eb.EB_BF16, dev_logits.data_ptr(), 0, TEMPERATURE,
+        st = lib.eb_sampler_step(pref, B, L, V, lk["eb"], dev_logits.data_ptr(), 0, TEMPERATURE,
                                  *ptrs, ws.data_ptr(), ws_bytes, sp)
         if st != 0:
             raise eb.EbError(st, lib.eb_last_error().decode())

@@ -15,7 +15,7 @@ import os
 from .build import LIB_PATH, build  # noqa: F401
 
 EB_OK, EB_ERR_INVALID, EB_ERR_CUDA, EB_ERR_UNSUPPORTED, EB_ERR_WORKSPACE, EB_ERR_CALLBACK = range(6)
-EB_F32, EB_BF16 = 0, 1
+EB_F32, EB_BF16, EB_FP8_E4M3 = 0, 1, 2
 EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
 EB_STATUS_TIMEOUT = 0x200

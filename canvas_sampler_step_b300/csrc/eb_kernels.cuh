@@ -309,6 +309,31 @@ __device__ __forceinline__ RowState empty_state()
     return RowState{kEmptyMax, 0.0f, 0.0f, 0x7FFFFFFF, -INFINITY, -1};
 }
 
+// ---------------------------------------------------------------- e4m3 logits
+
+// Four OCP e4m3 logits (byte i of w is entry i) as binary32.  Every e4m3 value, NaN included,
+// is exact in binary16 and binary16 is exact in binary32, so both conversions are exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float &x0, float &x1, float &x2, float &x3)
+{
+    asm("{\n\t.reg .b16 q0, q1, h0, h1, h2, h3;\n\t.reg .b32 p01, p23;\n\t"
+        "mov.b32 {q0, q1}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p01, q0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p23, q1;\n\t"
+        "mov.b32 {h0, h1}, p01;\n\t"
+        "mov.b32 {h2, h3}, p23;\n\t"
+        "cvt.f32.f16 %0, h0;\n\tcvt.f32.f16 %1, h1;\n\tcvt.f32.f16 %2, h2;\n\tcvt.f32.f16 %3, h3;\n\t}"
+        : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+        : "r"(w));
+}
+
+// One e4m3 logit (the low byte of b) as binary32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b)
+{
+    float x0, x1, x2, x3;
+    e4m3x4_to_f32(b & 0xFFu, x0, x1, x2, x3);
+    return x0;
+}
+
 // ---------------------------------------------------------------- packed per-vector body
 
 // Sums of one consumer thread over its part of a row, as two packed pairs each (four
@@ -561,21 +586,33 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
                                                PackedSums &q, float &nb, f32x2 &nb2, float &K,
                                                bool gumbel = true)
 {
-    float x[VEC];
-    if constexpr (VEC == 8) {
-        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[2 * i] = __uint_as_float(w4[i] << 16);
-            x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-        }
+    if constexpr (VEC == 16) {
+        // e4m3: the vector's two halves of 8 through the 8-entry body
+        float x[8], y[8];
+        e4m3x4_to_f32(r.x, x[0], x[1], x[2], x[3]);
+        e4m3x4_to_f32(r.y, x[4], x[5], x[6], x[7]);
+        e4m3x4_to_f32(r.z, y[0], y[1], y[2], y[3]);
+        e4m3x4_to_f32(r.w, y[4], y[5], y[6], y[7]);
+        consume_vals<8, MASKED, true>(x, valid, jvec * 16, a, rc, c2, st, q, nb, nb2, K, gumbel);
+        consume_vals<8, MASKED, true>(y, valid, jvec * 16 + 8, a, rc, c2, st, q, nb, nb2, K, gumbel);
+        return;
     } else {
-        x[0] = __uint_as_float(r.x);
-        x[1] = __uint_as_float(r.y);
-        x[2] = __uint_as_float(r.z);
-        x[3] = __uint_as_float(r.w);
+        float x[VEC];
+        if constexpr (VEC == 8) {
+            const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = __uint_as_float(w4[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+            }
+        } else {
+            x[0] = __uint_as_float(r.x);
+            x[1] = __uint_as_float(r.y);
+            x[2] = __uint_as_float(r.z);
+            x[3] = __uint_as_float(r.w);
+        }
+        consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, rc, c2, st, q, nb, nb2, K, gumbel);
     }
-    consume_vals<VEC, MASKED, true>(x, valid, jvec * VEC, a, rc, c2, st, q, nb, nb2, K, gumbel);
 }
 
 // Largest of N floats (N = 4, 8 or 16) with three-input maxima.
@@ -609,7 +646,12 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
     float x[N];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        if constexpr (VEC == 8) {
+        if constexpr (VEC == 16) {
+            e4m3x4_to_f32(r[u].x, x[16 * u + 0], x[16 * u + 1], x[16 * u + 2], x[16 * u + 3]);
+            e4m3x4_to_f32(r[u].y, x[16 * u + 4], x[16 * u + 5], x[16 * u + 6], x[16 * u + 7]);
+            e4m3x4_to_f32(r[u].z, x[16 * u + 8], x[16 * u + 9], x[16 * u + 10], x[16 * u + 11]);
+            e4m3x4_to_f32(r[u].w, x[16 * u + 12], x[16 * u + 13], x[16 * u + 14], x[16 * u + 15]);
+        } else if constexpr (VEC == 8) {
             const uint32_t w4[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -695,21 +737,28 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
             any |= cand[u];
         }
         if (__any_sync(0xFFFFFFFFu, any)) {
+            // the exact pass takes groups of up to 8 entries (two per e4m3 vector)
+            constexpr int G8 = VEC < 8 ? VEC : 8;
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (cand[u]) {
-                    const float4 xa = make_float4(x[VEC * u], x[VEC * u + 1], x[VEC * u + 2], x[VEC * u + 3]);
-                    const float4 xb = VEC == 8 ? make_float4(x[VEC * u + (VEC > 4 ? 4 : 0)], x[VEC * u + (VEC > 5 ? 5 : 0)],
-                                                             x[VEC * u + (VEC > 6 ? 6 : 0)], x[VEC * u + (VEC > 7 ? 7 : 0)])
-                                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    const uint4 wa = make_uint4(w[VEC * u], w[VEC * u + 1], w[VEC * u + 2], w[VEC * u + 3]);
-                    const uint4 wb = VEC == 8 ? make_uint4(w[VEC * u + (VEC > 4 ? 4 : 0)], w[VEC * u + (VEC > 5 ? 5 : 0)],
-                                                           w[VEC * u + (VEC > 6 ? 6 : 0)], w[VEC * u + (VEC > 7 ? 7 : 0)])
-                                              : make_uint4(0u, 0u, 0u, 0u);
-                    const GumbelBest g = gumbel_exact_group<VEC>(xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC,
-                                                                 rc.c, rc.invT, nb, K, GumbelBest{st.best, st.bi});
-                    st.best = g.score;
-                    st.bi = g.idx;
+#pragma unroll
+                    for (int h = 0; h < VEC / G8; ++h) {
+                        const int o = VEC * u + G8 * h;
+                        const float4 xa = make_float4(x[o], x[o + 1], x[o + 2], x[o + 3]);
+                        const float4 xb = G8 == 8 ? make_float4(x[o + (G8 > 4 ? 4 : 0)], x[o + (G8 > 5 ? 5 : 0)],
+                                                                x[o + (G8 > 6 ? 6 : 0)], x[o + (G8 > 7 ? 7 : 0)])
+                                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        const uint4 wa = make_uint4(w[o], w[o + 1], w[o + 2], w[o + 3]);
+                        const uint4 wb = G8 == 8 ? make_uint4(w[o + (G8 > 4 ? 4 : 0)], w[o + (G8 > 5 ? 5 : 0)],
+                                                              w[o + (G8 > 6 ? 6 : 0)], w[o + (G8 > 7 ? 7 : 0)])
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+                        const GumbelBest g = gumbel_exact_group<G8>(
+                            xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC + (uint32_t)(G8 * h), rc.c, rc.invT,
+                            nb, K, GumbelBest{st.best, st.bi});
+                        st.best = g.score;
+                        st.bi = g.idx;
+                    }
                 }
             warp_best(st.best, st.bi);
             K = cand_scale(st.xm, st.best, rc.c);

@@ -16,33 +16,14 @@
 
 namespace ebk {
 
-enum Kind { kF32Vec = 0, kBF16Vec = 1, kF32Scalar = 2, kBF16Scalar = 3 };
+enum Kind { kF32Vec = 0, kBF16Vec = 1, kF32Scalar = 2, kBF16Scalar = 3, kFP8Vec = 4, kFP8Scalar = 5 };
+constexpr int kKinds = 6;
 
+// Logits per 16-byte vector of a vector kind.
 template <int KIND> struct KindTraits;
-template <> struct KindTraits<kF32Vec> {
-    static constexpr int VEC = 4;
-    static __device__ __forceinline__ void unpack(const uint4 &r, float (&x)[4])
-    {
-        x[0] = __uint_as_float(r.x);
-        x[1] = __uint_as_float(r.y);
-        x[2] = __uint_as_float(r.z);
-        x[3] = __uint_as_float(r.w);
-    }
-};
-template <> struct KindTraits<kBF16Vec> {
-    static constexpr int VEC = 8;
-    static __device__ __forceinline__ void unpack(const uint4 &r, float (&x)[8])
-    {
-        x[0] = __uint_as_float(r.x << 16);
-        x[1] = __uint_as_float(r.x & 0xFFFF0000u);
-        x[2] = __uint_as_float(r.y << 16);
-        x[3] = __uint_as_float(r.y & 0xFFFF0000u);
-        x[4] = __uint_as_float(r.z << 16);
-        x[5] = __uint_as_float(r.z & 0xFFFF0000u);
-        x[6] = __uint_as_float(r.w << 16);
-        x[7] = __uint_as_float(r.w & 0xFFFF0000u);
-    }
-};
+template <> struct KindTraits<kF32Vec> { static constexpr int VEC = 4; };
+template <> struct KindTraits<kBF16Vec> { static constexpr int VEC = 8; };
+template <> struct KindTraits<kFP8Vec> { static constexpr int VEC = 16; };
 
 // Philox words of the VEC entries of vector jvec (entries jvec*VEC ..).  The word of entry
 // v is word v % 4 of counter (v / 4, p, s, stream << 24 | b).
@@ -246,7 +227,8 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, f
 // built.
 constexpr int kDirectThreads = 512;
 constexpr int kDirectWarps = kDirectThreads / 32;
-constexpr int kDirectU = 2;             // vectors per lane per batch
+constexpr int kDirectU = 2;             // vectors per lane per batch (binary32, bfloat16)
+constexpr int kFP8U = 1;                // ... and for e4m3, whose vectors hold 16 logits
 constexpr int kAsyncDepth = 4;          // batches in flight per lane
 constexpr int kDirectStageBytes = kAsyncDepth * kDirectU * kDirectThreads * 16;
 
@@ -452,7 +434,9 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
             float x[1] = {0.0f};
             if (valid) {
                 if (KIND == kF32Scalar) x[0] = __ldg(reinterpret_cast<const float *>(base) + v);
-                else x[0] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(base) + v) << 16);
+                else if (KIND == kBF16Scalar)
+                    x[0] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(base) + v) << 16);
+                else x[0] = e4m3_to_f32((uint32_t)__ldg(reinterpret_cast<const unsigned char *>(base) + v));
             }
             if (masked) consume_vec<1, true>(x, valid, v, a, rc, st, nb, K);
             else consume_vec<1, false>(x, valid, v, a, rc, st, nb, K);
@@ -826,7 +810,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Per-device launch geometry, filled once per device.
 struct DeviceGeometry {
     std::atomic<int> ready{0};
-    int grid[4] = {0, 0, 0, 0};   // CTAs of k1 for each element kind
+    int grid[ebk::kKinds] = {};   // CTAs of k1 for each element kind
 };
 DeviceGeometry g_geometry[64];
 
@@ -855,14 +839,18 @@ eb_status geometry(int *grid_out, int kind)
         if ((cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess ||
              cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess ||
+             cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kFP8Vec, ebk::kFP8U>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess))
             return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
         (void)smem_optin;
         // one CTA of kDirectWarps warps per SM; every warp is one unit of the row partition
         g.grid[ebk::kF32Vec] = nsm * ebk::kDirectWarps;
         g.grid[ebk::kBF16Vec] = nsm * ebk::kDirectWarps;
+        g.grid[ebk::kFP8Vec] = nsm * ebk::kDirectWarps;
         g.grid[ebk::kF32Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kF32Scalar>, ebk::kConsumers, 0, nsm);
         g.grid[ebk::kBF16Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kBF16Scalar>, ebk::kConsumers, 0, nsm);
+        g.grid[ebk::kFP8Scalar] = resident_ctas(ebk::k1_rowstats_scalar<ebk::kFP8Scalar>, ebk::kConsumers, 0, nsm);
         g.ready.store(1, std::memory_order_release);
     }
     *grid_out = g.grid[kind];
@@ -1020,7 +1008,8 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
     if (B < 0) return fail(EB_ERR_INVALID, "B must be >= 0 (got %d)", B);
     if (L < 1 || L > ebk::kMaxL) return fail(EB_ERR_INVALID, "L must be in [1, %d] (got %d)", ebk::kMaxL, L);
     if (V < 1) return fail(EB_ERR_INVALID, "V must be >= 1 (got %d)", V);
-    if (dtype != EB_F32 && dtype != EB_BF16) return fail(EB_ERR_INVALID, "unknown dtype %d", (int)dtype);
+    if (dtype != EB_F32 && dtype != EB_BF16 && dtype != EB_FP8_E4M3)
+        return fail(EB_ERR_INVALID, "unknown dtype %d", (int)dtype);
     if (B == 0) return EB_OK;
     if (!d_logits) return fail(EB_ERR_INVALID, "d_logits is NULL");
     if (!sb.mask || !sb.tokens || !sb.prev_argmax || !sb.status || !sb.entropy || !sb.argmax ||
@@ -1099,12 +1088,13 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
                       const void *d_logits, int step, float T, const StepBuffers &sb,
                       void *d_ws, cudaStream_t stream)
 {
-    const size_t esize = dtype == EB_F32 ? 4 : 2;
+    const size_t esize = dtype == EB_F32 ? 4 : (dtype == EB_BF16 ? 2 : 1);
     const bool aligned = (((uintptr_t)d_logits & 15) == 0) && (((size_t)V * esize) % 16 == 0);
     int kind;
     if (dtype == EB_F32) kind = aligned ? ebk::kF32Vec : ebk::kF32Scalar;
-    else kind = aligned ? ebk::kBF16Vec : ebk::kBF16Scalar;
-    const int vec = kind == ebk::kF32Vec ? 4 : (kind == ebk::kBF16Vec ? 8 : 1);
+    else if (dtype == EB_BF16) kind = aligned ? ebk::kBF16Vec : ebk::kBF16Scalar;
+    else kind = aligned ? ebk::kFP8Vec : ebk::kFP8Scalar;
+    const int vec = aligned ? (int)(16 / esize) : 1;
     int gmax = 0;
     eb_status st = geometry(&gmax, kind);
     if (st != EB_OK) return st;
@@ -1155,8 +1145,13 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
         ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>
             <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
         break;
+    case ebk::kFP8Vec:
+        ebk::k1_rowstats_direct<ebk::kFP8Vec, ebk::kFP8U>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
+        break;
     case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
-    default: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    case ebk::kBF16Scalar: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    default: ebk::k1_rowstats_scalar<ebk::kFP8Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(EB_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));

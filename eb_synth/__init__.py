@@ -216,6 +216,41 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((bits + bias) >> np.uint32(16)).astype(np.uint16)
 
 
+def to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round binary32 to OCP FP8 e4m3 (nearest, ties to even; magnitudes above the largest
+    finite value 448 saturate to it; NaN stays NaN), returned as uint8 codes.  Normal codes
+    hold (1 + m/8) 2^(e-7) for exponent field e in 1..15 (m < 7 when e = 15); subnormal codes
+    m/8 2^-6, so below 2^-6 the grid is 2^-9."""
+    x = np.ascontiguousarray(x, _F)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    a = np.abs(x).astype(np.float64)                       # exact
+    a = np.where(np.isfinite(a), a, 1e6)                   # inf / NaN: fixed up below
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    # correct log2's rounding at exact powers of two
+    e = np.where(np.ldexp(1.0, e.astype(np.int64)) > a, e - 1, e)
+    e = np.where(np.ldexp(1.0, (e + 1).astype(np.int64)) <= a, e + 1, e)
+    e = np.maximum(e, -6.0)                                  # the subnormal grid below 2^-6
+    q = np.rint(np.ldexp(a, (3 - e).astype(np.int64)))       # 8..16 (normal) or 0..8 (subnormal)
+    e = np.where(q >= 16, e + 1, e)
+    q = np.where(q >= 16, q / 2, q)
+    normal = q >= 8
+    code = np.where(normal, ((e + 7) * 8 + (q - 8)), q)
+    code = np.where(a > 448.0, 0x7E, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return (code.astype(np.uint8) | np.where(np.isnan(x), np.uint8(0), sign)).astype(np.uint8)
+
+
+def e4m3_bits_to_f32(c: np.ndarray) -> np.ndarray:
+    """Exact binary32 values of e4m3 codes (NaN for S.1111.111)."""
+    c = np.asarray(c, np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e, m = (c >> 3) & 15, c & 7
+    v = np.where(e == 0, np.ldexp(m.astype(np.float64), -9), np.ldexp((8 + m).astype(np.float64), e - 10))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return (s * v).astype(_F)
+
+
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.asarray(h, np.uint16).astype(np.uint32) << np.uint32(16)).view(_F)
 
@@ -226,7 +261,7 @@ class Peaked:
     B: int
     L: int
     V: int
-    dtype: str            # "f32" or "bf16"
+    dtype: str            # "f32", "bf16" or "fp8" (e4m3)
     sigma: float
     base_lo: float
     base_scale: float
@@ -249,11 +284,14 @@ class Peaked:
         h = self.peak_height(b, u, s)
         idx = np.arange(p.shape[0])
         x[idx, t[p]] = x[idx, t[p]] + h[p]
-        return to_bf16_bits(x) if self.dtype == "bf16" else x
+        if self.dtype == "bf16":
+            return to_bf16_bits(x)
+        return to_e4m3_bits(x) if self.dtype == "fp8" else x
 
     def logits(self, s: int, rows_per_chunk: int = 16) -> np.ndarray:
         """Full logits [B, L, V] at step s."""
-        out = np.empty((self.B, self.L, self.V), np.uint16 if self.dtype == "bf16" else _F)
+        dt = {"bf16": np.uint16, "fp8": np.uint8}.get(self.dtype, _F)
+        out = np.empty((self.B, self.L, self.V), dt)
         for b in range(self.B):
             for p0 in range(0, self.L, rows_per_chunk):
                 p = np.arange(p0, min(self.L, p0 + rows_per_chunk))

@@ -116,6 +116,29 @@ __device__ __forceinline__ uint16_t to_bf16(float x)
     return (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);
 }
 
+// Binary32 to OCP FP8 e4m3: nearest, ties to even; magnitudes above 448 (the largest finite
+// value) saturate to it; NaN becomes 0x7F.  The same steps as the numpy generator's: the
+// exponent e = floor(log2 |x|) (at least -6, the subnormal grid), q = rint(|x| 2^(3 - e)) in
+// 0..16, a carry of q = 16 into the exponent, then code (e + 7) 8 + q - 8 (q >= 8) or q.
+__device__ __forceinline__ uint32_t to_e4m3(float x)
+{
+    const uint32_t bits = __float_as_uint(x);
+    if (isnan(x)) return 0x7Fu;
+    const uint32_t sign = (bits >> 24) & 0x80u;
+    const float a = fabsf(x);
+    if (a > 448.0f) return sign | 0x7Eu;
+    int e = (int)((bits >> 23) & 0xFFu) - 127;
+    if (e < -6) e = -6;
+    const float scale = __int_as_float((127 + 3 - e) << 23);     // 2^(3 - e), exact
+    int q = (int)rintf(__fmul_rn(a, scale));
+    if (q >= 16) {
+        e += 1;
+        q >>= 1;
+    }
+    const uint32_t code = q >= 8 ? (uint32_t)((e + 7) * 8 + (q - 8)) : (uint32_t)q;
+    return sign | code;
+}
+
 constexpr int kThreads = 256;
 constexpr int kGroupsPerThread = 8;
 
@@ -173,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) peaked_logits_kernel(const eb_synth_
                 for (int j = 0; j < 4; ++j)
                     if (4 * k + j < r.V) o[base + j] = x[j];
             }
-        } else {
+        } else if (r.dtype == 1) {
             uint16_t *o = static_cast<uint16_t *>(out);
             if (vec) {
                 const uint32_t lo = (uint32_t)to_bf16(x[0]) | ((uint32_t)to_bf16(x[1]) << 16);
@@ -182,6 +205,16 @@ __global__ void __launch_bounds__(kThreads) peaked_logits_kernel(const eb_synth_
             } else {
                 for (int j = 0; j < 4; ++j)
                     if (4 * k + j < r.V) o[base + j] = to_bf16(x[j]);
+            }
+        } else {
+            uint8_t *o = static_cast<uint8_t *>(out);
+            if (vec) {
+                const uint32_t w = to_e4m3(x[0]) | (to_e4m3(x[1]) << 8) | (to_e4m3(x[2]) << 16) |
+                                   (to_e4m3(x[3]) << 24);
+                *reinterpret_cast<uint32_t *>(o + base) = w;
+            } else {
+                for (int j = 0; j < 4; ++j)
+                    if (4 * k + j < r.V) o[base + j] = (uint8_t)to_e4m3(x[j]);
             }
         }
     }
@@ -228,7 +261,7 @@ int eb_synth_logits(const eb_synth_recipe *r, int step, const int32_t *d_status,
                     void *stream)
 {
     if (!r || !d_logits || r->B < 0 || r->B > EB_SYNTH_MAX_B || r->L < 1 || r->V < 1 ||
-        (r->dtype != 0 && r->dtype != 1) || step < 0 || (long long)r->B * r->L > 65535)
+        (r->dtype < 0 || r->dtype > 2) || step < 0 || (long long)r->B * r->L > 65535)
         return 1;
     if (r->B == 0) return 0;
     const long long nk = ((long long)r->V + 3) / 4;
@@ -243,7 +276,7 @@ int eb_synth_slot_logits(const eb_synth_recipe *r, int B_slots, const int32_t *d
                          const int32_t *d_slot_step, void *d_logits, void *stream)
 {
     if (!r || !d_logits || !d_slot_block || !d_slot_step || r->B < 1 || r->B > EB_SYNTH_MAX_B ||
-        r->L < 1 || r->V < 1 || (r->dtype != 0 && r->dtype != 1) || B_slots < 0 ||
+        r->L < 1 || r->V < 1 || (r->dtype < 0 || r->dtype > 2) || B_slots < 0 ||
         (long long)B_slots * r->L > 65535)
         return 1;
     if (B_slots == 0) return 0;

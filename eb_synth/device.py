@@ -37,7 +37,7 @@ class Recipe(ctypes.Structure):
             raise ValueError(f"B={cfg.B} > {MAX_B}")
         r = Recipe()
         r.B, r.L, r.V = cfg.B, cfg.L, cfg.V
-        r.dtype = 1 if cfg.dtype == "bf16" else 0
+        r.dtype = {"f32": 0, "bf16": 1, "fp8": 2}[cfg.dtype]
         r.sigma, r.base_lo, r.base_scale = cfg.sigma, cfg.base_lo, cfg.base_scale
         for b in range(cfg.B):
             r.growth[b] = cfg.growth[b]

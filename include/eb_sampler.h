@@ -58,7 +58,9 @@ typedef enum {
     EB_ERR_CALLBACK = 5      /* the logits callback of eb_sample_canvas returned non-zero */
 } eb_status;
 
-typedef enum { EB_F32 = 0, EB_BF16 = 1 } eb_dtype;
+/* Logit element types: binary32, bfloat16, and OCP FP8 e4m3 (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN) for the streaming entry points. */
+typedef enum { EB_F32 = 0, EB_BF16 = 1, EB_FP8_E4M3 = 2 } eb_dtype;
 
 /* Canvas status word d_status[b]: the low byte is the stop reason. */
 #define EB_RUNNING 0
@@ -118,7 +120,7 @@ size_t eb_workspace_bytes(int B, int L, int V, eb_dtype dtype);
  *
  *   params         sampler settings (host pointer, read during the call only)
  *   B, L, V        canvases, positions per canvas (1..1024), vocabulary (1..2^31-1)
- *   dtype          element type of d_logits (EB_F32 or EB_BF16)
+ *   dtype          element type of d_logits (EB_F32, EB_BF16 or EB_FP8_E4M3)
  *   d_logits       [B, L, V] logits of this step (read only)
  *   step           denoising step index s (0-based, < params->max_steps); keys the
  *                  Gumbel noise and the stop / cap rules

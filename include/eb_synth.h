@@ -10,7 +10,8 @@
  * 2 << 24 | b)), and t_p = (w0 * V) >> 32, u_p = ((w1 >> 9) + 1/2) 2^-23 from the words of
  * counter (0, p, 0, 3 << 24 | b).  Every binary32 operation is rounded to nearest even in a
  * fixed order (no fused multiply-add), so the values are bit-identical to the numpy
- * generator of the eb_synth Python package.
+ * generator of the eb_synth Python package; bfloat16 rounds to nearest even, e4m3 to nearest
+ * even with saturation at 448.
  *
  * Pointers prefixed d_ are device memory owned by the caller; `stream` is a cudaStream_t
  * passed as void*.  Functions return 0 on success, non-zero on a bad argument or a CUDA
@@ -29,7 +30,7 @@ extern "C" {
 
 typedef struct {
     int32_t B, L, V;
-    int32_t dtype;                       /* 0 = binary32, 1 = bfloat16 */
+    int32_t dtype;                       /* 0 = binary32, 1 = bfloat16, 2 = FP8 e4m3 */
     float sigma, base_lo, base_scale;
     float growth[EB_SYNTH_MAX_B];        /* per canvas */
     uint64_t seed[EB_SYNTH_MAX_B];       /* per canvas */

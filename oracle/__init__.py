@@ -40,7 +40,7 @@ _SRC = os.path.join(_HERE, "eb_oracle.c")
 _LIB = os.path.join(_HERE, "libeb_oracle.so")
 
 RUNNING, ADAPTIVE, COMPLETE, CAP = 0, 1, 2, 3
-DTYPE_F32, DTYPE_BF16, DTYPE_F64 = 0, 1, 2
+DTYPE_F32, DTYPE_BF16, DTYPE_F64, DTYPE_E4M3 = 0, 1, 2, 3
 
 _lib = None
 
@@ -83,6 +83,8 @@ def _load():
                                    ctypes.c_uint32, P,
                                    P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.eb_oracle_step.restype = None
+    lib.eb_oracle_e4m3_value.argtypes = [ctypes.c_int]
+    lib.eb_oracle_e4m3_value.restype = ctypes.c_double
     lib.eb_oracle_num_threads.argtypes = []
     lib.eb_oracle_num_threads.restype = ctypes.c_int
     lib.eb_oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -131,7 +133,7 @@ _schedule = temperature
 
 
 def _logits_array(x: np.ndarray):
-    """Accepts float32, float64, or bfloat16 carried as uint16 bits."""
+    """Accepts float32, float64, bfloat16 carried as uint16 bits, or e4m3 codes as uint8."""
     x = np.ascontiguousarray(x)
     if x.dtype == np.float32:
         return x, DTYPE_F32
@@ -139,7 +141,14 @@ def _logits_array(x: np.ndarray):
         return x, DTYPE_BF16
     if x.dtype == np.float64:
         return x, DTYPE_F64
-    raise TypeError(f"logits must be float32, float64 or uint16 (bf16 bits), got {x.dtype}")
+    if x.dtype == np.uint8:
+        return x, DTYPE_E4M3
+    raise TypeError(f"logits must be float32, float64, uint16 (bf16 bits) or uint8 (e4m3 codes), got {x.dtype}")
+
+
+def e4m3_value(code: int) -> float:
+    """Exact value of one OCP FP8 e4m3 code (NaN for S.1111.111)."""
+    return float(_load().eb_oracle_e4m3_value(int(code)))
 
 
 def row(x: np.ndarray, T: float, masked: bool, seed: int = 0, b: int = 0, p: int = 0, s: int = 0):

@@ -111,8 +111,20 @@ double eb_oracle_temperature(int step, int max_steps, double t_start, double t_e
     return t_start + (t_end - t_start) * (double)step / (double)(max_steps - 1);
 }
 
+/* Value of one OCP FP8 e4m3 code: sign s, exponent field e (bias 7), mantissa m (3 bits);
+ * e = 0 is subnormal, m / 8 * 2^-6; S.1111.111 is NaN; there are no infinities. */
+static double e4m3_value(uint8_t code)
+{
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(8.0 + (double)m, e - 10);
+    return s ? -v : v;
+}
+
 /* Exact conversion of one logit to binary64. dtype: 0 = binary32, 1 = bfloat16 bits,
- * 2 = binary64. */
+ * 2 = binary64, 3 = e4m3 codes. */
 static double load_logit(const void *x, int dtype, int64_t i)
 {
     if (dtype == 0) return (double)((const float *)x)[i];
@@ -122,8 +134,12 @@ static double load_logit(const void *x, int dtype, int64_t i)
         memcpy(&f, &bits, sizeof f);
         return (double)f;
     }
+    if (dtype == 3) return e4m3_value(((const uint8_t *)x)[i]);
     return ((const double *)x)[i];
 }
+
+/* The e4m3 decoding above, exported for the tests. */
+double eb_oracle_e4m3_value(int code) { return e4m3_value((uint8_t)code); }
 
 /* One canvas row of V logits at temperature T.
  * Outputs: H = softmax entropy of z = x/T in nats; A = first index of the largest raw
@@ -283,7 +299,7 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
 {
     double T = temperature > 0.0 ? temperature
                                  : eb_oracle_temperature(step, max_steps, t_start, t_end);
-    size_t esize = dtype == 0 ? 4 : (dtype == 1 ? 2 : 8);
+    size_t esize = dtype == 0 ? 4 : (dtype == 1 ? 2 : (dtype == 3 ? 1 : 8));
     int64_t rows = (int64_t)B * L;
 
     #pragma omp parallel for schedule(dynamic, 1)

@@ -119,7 +119,7 @@ def params_pair(seed=0, **kw):
 
 
 def device_logits(cfg: eb_synth.Peaked, step: int, status=None) -> torch.Tensor:
-    dt = torch.float32 if cfg.dtype == "f32" else torch.int16
+    dt = {"f32": torch.float32, "bf16": torch.int16, "fp8": torch.uint8}[cfg.dtype]
     out = torch.empty((cfg.B, cfg.L, cfg.V), dtype=dt, device="cuda")
     synth_dev.logits(synth_dev.Recipe.of(cfg), step, out, status)
     return out

@@ -29,7 +29,7 @@ def _ready():
 
 
 def _dtype(cfg):
-    return eb.EB_BF16 if cfg.dtype == "bf16" else eb.EB_F32
+    return {"f32": eb.EB_F32, "bf16": eb.EB_BF16, "fp8": eb.EB_FP8_E4M3}[cfg.dtype]
 
 
 # ------------------------------------------------------------------ generator
@@ -40,16 +40,17 @@ def _dtype(cfg):
     (eb_synth.Peaked(2, 5, 1001, "f32", 3.0, 1.0, 2.0, (0.3, 0.7), (11, 12)), None),
     (eb_synth.Peaked(2, 5, 1001, "bf16", 3.0, 1.0, 2.0, (0.3, 0.7), (11, 12)), None),
     (eb_synth.cfg3(B=8, L=256, V=262144), [0, 77, 255]),
+    (eb_synth.Peaked(2, 5, 1001, "fp8", 3.0, 1.0, 2.0, (0.3, 0.7), (11, 12)), None),
+    (eb_synth.Peaked(1, 4, 65536, "fp8", 60.0, 400.0, 200.0, (0.0,), (13,)), None),   # saturation
 ])
 def test_generator_bit_exact(cfg, rows):
+    view = {"f32": np.uint32, "bf16": np.uint16, "fp8": np.uint8}[cfg.dtype]
     for s in (0, 7):
         dev = device_logits(cfg, s).cpu().numpy()
         for b in range(cfg.B):
             p = np.arange(cfg.L) if rows is None else np.array(rows)
             host = cfg.rows(b, p, s)
-            got = dev[b, p].view(np.uint16) if cfg.dtype == "bf16" else dev[b, p]
-            assert np.array_equal(got.view(np.uint32 if cfg.dtype == "f32" else np.uint16),
-                                  host.view(np.uint32 if cfg.dtype == "f32" else np.uint16)), (b, s)
+            assert np.array_equal(dev[b, p].view(view), host.view(view)), (b, s)
 
 
 def test_generator_skips_stopped_canvases():
@@ -85,6 +86,10 @@ CASES = [
     # scalar paths: V not a multiple of the 16-byte vector
     (eb_synth.Peaked(2, 16, 4099, "f32", 3.0, 2.0, 0.0, (0.3, 0.3), (6, 7)), 3, 1.0),
     (eb_synth.Peaked(1, 40, 12347, "bf16", 2.5, 0.0, 12.0, (0.0,), (8,)), 0, 0.5),
+    # e4m3 logits: 16 per vector, a ragged tail (20000 = 1250 vectors), and the scalar path
+    (eb_synth.Peaked(2, 64, 4096, "fp8", 2.5, 0.0, 12.0, (0.0, 0.0), (14, 15)), 0, 0.5),
+    (eb_synth.Peaked(2, 48, 20000, "fp8", 3.0, 4.0, 2.0, (0.3, 0.3), (16, 17)), 12, 0.8),
+    (eb_synth.Peaked(1, 32, 4099, "fp8", 3.0, 2.0, 0.0, (0.3,), (18,)), 3, 1.0),
     # tiny rows and a non-power-of-two canvas
     (eb_synth.Peaked(1, 1000, 8, "f32", 1.0, 3.0, 0.0, (0.0,), (9,)), 2, 0.9),
     (eb_synth.Peaked(4, 1, 1, "f32", 1.0, 0.0, 0.0, (0.0,) * 4, (1, 2, 3, 4)), 0, 1.0),
@@ -126,6 +131,25 @@ def test_step_parity_single_step_workload_full_size(seed):
     res = oracle.step(x, ost, 0, op, temperature=float(np.float32(0.8)))
     rep = Report()
     compare_step(host_state(c), res, ost, np.array([True]), rep, ctx=f"seed {seed}")
+    assert rep.max_h_err < H_TOL
+
+
+def test_step_parity_single_step_workload_e4m3_full_size():
+    """The benchmarked step with its logits rounded to e4m3 (64 MiB): only about 250 distinct
+    values, so most argmax comparisons are exact ties that the first index settles."""
+    import dataclasses
+    cfg = dataclasses.replace(eb_synth.cfg1(0), dtype="fp8")
+    mask = eb_synth.cfg1_mask(0)
+    x = cfg.logits(0)
+    dev = device_logits(cfg, 0)
+    assert np.array_equal(dev.cpu().numpy(), x)
+    gp, op = params_pair(seed=0)
+    c = eb.Canvas(1, 256, 262144, eb.EB_FP8_E4M3, mask=mask)
+    ost = oracle.State.fresh(1, 256, mask)
+    c.step(gp, dev, 0, 0.8)
+    res = oracle.step(x, ost, 0, op, temperature=float(np.float32(0.8)))
+    rep = Report()
+    compare_step(host_state(c), res, ost, np.array([True]), rep, ctx="e4m3")
     assert rep.max_h_err < H_TOL
 
 

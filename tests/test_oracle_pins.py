@@ -439,3 +439,28 @@ def test_blocks_run_alone_equal_the_batch_loop():
     r_batch = oracle.step(cfg.logits(0)[:2], oracle.State.fresh(2, 16), 0, op)
     assert np.array_equal(r_own.Y[0], r_batch.Y[1])
     assert (r_own.Y[0] != r_zero.Y[0]).sum() >= 4
+
+
+# ---------------------------------------------------------------- e4m3 logits
+
+def test_e4m3_decoding_known_values():
+    """OCP FP8 e4m3: bias 7, 3 mantissa bits, subnormals below 2^-6, no infinities,
+    S.1111.111 is NaN."""
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0x77: 240.0, 0xB8: -1.0,
+             0xFE: -448.0}
+    for code, value in known.items():
+        assert oracle.e4m3_value(code) == value, hex(code)
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    assert math.copysign(1.0, oracle.e4m3_value(0x80)) == -1.0
+
+
+def test_e4m3_row_equals_its_decoded_values():
+    """A row of e4m3 codes gives exactly the statistics of the binary64 values they encode."""
+    from eb_synth import e4m3_bits_to_f32
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 256, 4096).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C                     # no NaN in this row
+    a = oracle.row(codes, 0.8, True, 3, 0, 7, 2)
+    b = oracle.row(e4m3_bits_to_f32(codes).astype(np.float64), 0.8, True, 3, 0, 7, 2)
+    assert a[0] == b[0] and a[1] == b[1] and a[2] == b[2]

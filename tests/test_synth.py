@@ -76,3 +76,39 @@ def test_rows_subset_equals_full():
     full = cfg.logits(7)
     sub = cfg.rows(0, np.array([2, 9, 15]), 7)
     assert np.array_equal(full[0, [2, 9, 15]], sub)
+
+
+def test_e4m3_rounding_matches_torch_inside_the_range():
+    """Nearest-even rounding to e4m3 agrees with torch's float8_e4m3fn cast wherever no
+    saturation is involved (|x| <= 448), subnormals included."""
+    rng = np.random.default_rng(2)
+    x = np.concatenate([(rng.standard_normal(200000) * 40).astype(np.float32),
+                        (rng.standard_normal(50000) * 0.01).astype(np.float32),
+                        np.float32([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 1.0625, 232.0])])
+    x = x[np.abs(x) <= 448]
+    ours = S.to_e4m3_bits(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (ours == ref).all()
+
+
+def test_e4m3_rounding_by_brute_force_and_saturation():
+    """Against the definition: the nearest finite e4m3 value, ties to the even code; above 448
+    saturation; every finite code round-trips."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = S.e4m3_bits_to_f32(codes).astype(np.float64)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(S.to_e4m3_bits(vals[finite].astype(np.float32))[vals[finite] != 0],
+                          codes[finite][vals[finite] != 0])
+    fc, fv = codes[finite], vals[finite]
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-0.05, 0.05, 20000)]).astype(np.float32)
+    got = S.to_e4m3_bits(x)
+    for xi, gi in zip(x[:4000].astype(np.float64), got[:4000]):
+        d = np.abs(fv - xi)
+        best = np.nonzero(d == d.min())[0]
+        cand = fc[best]
+        if len(cand) > 1:                      # a tie: the even mantissa, the same sign as x
+            cand = [c for c in cand if (c & 1) == 0 and ((c >> 7) == (xi < 0) or (c & 0x7F) == 0)]
+        assert gi in cand or (gi & 0x7F) == 0 and xi == 0
+    sat = S.to_e4m3_bits(np.float32([449.0, 464.0, 1e6, np.inf, -500.0, -np.inf, np.nan]))
+    assert sat.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]

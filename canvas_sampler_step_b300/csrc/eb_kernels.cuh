@@ -586,17 +586,8 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
                                                PackedSums &q, float &nb, f32x2 &nb2, float &K,
                                                bool gumbel = true)
 {
-    if constexpr (VEC == 16) {
-        // e4m3: the vector's two halves of 8 through the 8-entry body
-        float x[8], y[8];
-        e4m3x4_to_f32(r.x, x[0], x[1], x[2], x[3]);
-        e4m3x4_to_f32(r.y, x[4], x[5], x[6], x[7]);
-        e4m3x4_to_f32(r.z, y[0], y[1], y[2], y[3]);
-        e4m3x4_to_f32(r.w, y[4], y[5], y[6], y[7]);
-        consume_vals<8, MASKED, true>(x, valid, jvec * 16, a, rc, c2, st, q, nb, nb2, K, gumbel);
-        consume_vals<8, MASKED, true>(y, valid, jvec * 16 + 8, a, rc, c2, st, q, nb, nb2, K, gumbel);
-        return;
-    } else {
+    static_assert(VEC == 4 || VEC == 8, "e4m3 tails go through consume_vals in half vectors");
+    {
         float x[VEC];
         if constexpr (VEC == 8) {
             const uint32_t w4[4] = {r.x, r.y, r.z, r.w};

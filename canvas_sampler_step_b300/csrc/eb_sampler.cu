@@ -241,6 +241,16 @@ __device__ __forceinline__ uint64_t evict_first_policy()
     return pol;
 }
 
+// Plain 8-byte load (the e4m3 tail), bypassing L1, evict-first in L2.
+__device__ __forceinline__ uint2 ld_stream8(const uint2 *p)
+{
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p), "l"(evict_first_policy()));
+    return r;
+}
+
 // Plain 16-byte load of the ragged tail of a segment (bypassing L1, evict-first in L2).
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 {
@@ -344,12 +354,28 @@ __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src,
         if (gumbel) async_batches<VEC, U, true>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
         else async_batches<VEC, U, false>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
     }
+    if constexpr (VEC == 16) {
+        // e4m3: the tail in half vectors of 8 logits, consecutive half vectors on consecutive
+        // lanes, so that the lanes' entries stay in index order (first index on ties)
+        const uint2 *src2 = reinterpret_cast<const uint2 *>(src);
 #pragma unroll 1
-    for (uint32_t jb = jf; jb < j1; jb += 32u) {
-        const uint32_t idx = jb + lane;
-        const bool valid = idx < j1;
-        const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-        consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
+        for (uint32_t hb = 2u * jf; hb < 2u * j1; hb += 32u) {
+            const uint32_t h = hb + lane;
+            const bool valid = h < 2u * j1;
+            const uint2 r = valid ? ld_stream8(src2 + h) : make_uint2(0u, 0u);
+            float x[8];
+            e4m3x4_to_f32(r.x, x[0], x[1], x[2], x[3]);
+            e4m3x4_to_f32(r.y, x[4], x[5], x[6], x[7]);
+            consume_vals<8, true, true>(x, valid, h * 8u, a, rc, c2, st, q, nb, nb2, K, gumbel);
+        }
+    } else {
+#pragma unroll 1
+        for (uint32_t jb = jf; jb < j1; jb += 32u) {
+            const uint32_t idx = jb + lane;
+            const bool valid = idx < j1;
+            const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+            consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
+        }
     }
 }
 

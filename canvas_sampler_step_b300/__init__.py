@@ -23,6 +23,7 @@ EB_SLOT_IDLE = 0x400
 EB_FLAG_DIAG_STALL = 1
 EB_FLAG_STOP_MASKED_ONLY = 2
 EB_FLAG_FINALIZE_SAMPLED = 4
+EB_FLAG_STOP_RAW_ENTROPY = 8
 
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",

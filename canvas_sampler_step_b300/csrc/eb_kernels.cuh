@@ -114,6 +114,7 @@ struct K1Args {
     const int32_t *canvas_id;
     const float *canvas_c;
     const float *canvas_invT;
+    int raw;                // 1: every row as unmasked (no sampling), for the raw-logit entropy
 };
 
 struct K2Args {
@@ -148,6 +149,12 @@ struct K2Args {
     const float *canvas_c;       // per-canvas c, or null (then `c`)
     int stop_masked_only;      // EB_FLAG_STOP_MASKED_ONLY
     int finalize_sampled;      // EB_FLAG_FINALIZE_SAMPLED
+    // EB_FLAG_STOP_RAW_ENTROPY: partial states of a second pass over the same logits at T = 1
+    // (all rows unmasked, its own partition); the stop statistic then sums their entropies
+    const Partial *raw_partials;
+    const uint32_t *raw_prefix;
+    const int2 *raw_rowunits;
+    int raw_G, raw_weighted;
     int k3_g;                  // > 0: partials come from the fused unembedding kernel, whose
                                // row block mb, group rank j < k3_g and column group hh <
                                // k3_groups write slot ((mb k3_g + j) k3_groups + hh) 128 + row % 128

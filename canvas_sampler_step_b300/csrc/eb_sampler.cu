@@ -145,7 +145,7 @@ __device__ void build_prefix(const K1Args &a, uint32_t *P, uint8_t *mflag, uint3
     for (int k = 0; k < per; ++k) {
         const int r = r0 + k;
         if (r >= a.rows) break;
-        const uint8_t m = a.mask[r] ? 1 : 0;
+        const uint8_t m = (!a.raw && a.mask[r]) ? 1 : 0;
         mflag[r] = m;
         const bool active = a.status[r / a.L] == EB_RUNNING;
         const uint32_t w = active ? (uint32_t)a.nvec_row * (uint32_t)(m ? kWeightMasked : kWeightUnmasked) : 0u;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
         const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
         const f32x2 c2 = pk2(rc.c, rc.c);
-        const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
+        const bool masked = !a.raw && (a.weighted ? mflag[row] != 0 : a.mask[row] != 0);
         const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.logits) +
                                                            (size_t)row * (size_t)a.row_bytes);
         RowState st = empty_state();
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
         const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
-        const bool masked = a.weighted ? mflag[row] != 0 : a.mask[row] != 0;
+        const bool masked = !a.raw && (a.weighted ? mflag[row] != 0 : a.mask[row] != 0);
         const char *base = static_cast<const char *>(a.logits) + (size_t)row * (size_t)a.row_bytes;
         RowState st = empty_state();
         float nb = -st.xm * rc.c;
@@ -511,6 +511,46 @@ __device__ __forceinline__ unsigned long long entropy_key(float H, int p)
 // (fixed point) come first in (H, p) order, so only they need sorting, followed by the
 // lowest-entropy position above the bound, which is accepted iff every low one was and
 // their sum stays within the bound.  No later position can be accepted.
+// Merges the partial states of row r in slot order: the fused kernel's (group rank, column
+// group) slots when k3_g > 0, else the streaming units u.x .. u.y of `rowunits`.  W and G: the
+// streaming partition's total weight and unit count (a unit whose weight range is empty wrote
+// nothing, only when W < G).
+__device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *partials, const int2 *rowunits,
+                                             unsigned long long W, unsigned long long G, long long r, float c,
+                                             RowState &st, int &flags)
+{
+    long long base, stride;
+    int n;
+    if (a.k3_g > 0) {
+        const long long mb = r >> 7, rl = r & 127;
+        base = mb * a.k3_g * a.k3_groups * 128 + rl;
+        stride = 128;
+        n = a.k3_groups * a.k3_g;
+    } else {
+        const int2 u = rowunits[r];
+        base = r + u.x;
+        stride = 1;
+        n = u.y - u.x + 1;
+    }
+    // loads in batches of kMergeBatch independent requests, merged in slot order
+    for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
+        Partial q[kMergeBatch];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k)
+            if (i0 + k < n) q[k] = partials[base + (long long)(i0 + k) * stride];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            if (i0 + k >= n) break;
+            if (a.k3_g == 0 && W < G) {
+                const unsigned long long cu = (unsigned long long)(base - r + i0 + k);
+                if (cu * W / G >= (cu + 1) * W / G) continue;
+            }
+            merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, c);
+            flags |= q[k].flags;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
 {
     __shared__ unsigned long long Hq[kMaxL];     // entropies in 2^-40 nats
@@ -553,6 +593,10 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const unsigned long long W = k2_row_start(a, a.rows);
     const unsigned long long G = (unsigned long long)a.G;
+    const unsigned long long Wr = !a.raw_partials ? 0ull
+                                  : a.raw_weighted ? (unsigned long long)a.raw_prefix[a.rows]
+                                                   : (unsigned long long)a.rows * (unsigned long long)a.nvec_row;
+    const unsigned long long Gr = (unsigned long long)a.raw_G;
     __syncthreads();
 
     // 1. merge each row's partials (ascending CTA) -> H, A, Y
@@ -562,40 +606,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const long long r = rowbase + p;
         RowState st = empty_state();
         int flags = 0;
-        // slot list of row r in merge order: [n0, n1) of the fused kernel's (group rank,
-        // column half) pairs, or the row-statistics units u.x .. u.y
-        long long base, stride;
-        int n;
-        if (a.k3_g > 0) {
-            const long long mb = r >> 7, rl = r & 127;
-            base = mb * a.k3_g * a.k3_groups * 128 + rl;
-            stride = 128;
-            n = a.k3_groups * a.k3_g;
-        } else {
-            const int2 u = a.rowunits[r];
-            base = r + u.x;
-            stride = 1;
-            n = u.y - u.x + 1;
-        }
-        // loads in batches of kMergeBatch independent requests, merged in slot order
-        for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
-            Partial q[kMergeBatch];
-#pragma unroll
-            for (int k = 0; k < kMergeBatch; ++k)
-                if (i0 + k < n) q[k] = a.partials[base + (long long)(i0 + k) * stride];
-#pragma unroll
-            for (int k = 0; k < kMergeBatch; ++k) {
-                if (i0 + k >= n) break;
-                // a streaming unit whose weight range is empty wrote nothing (only when the
-                // total weight is below the unit count)
-                if (a.k3_g == 0 && W < G) {
-                    const unsigned long long c = (unsigned long long)(base - r + i0 + k);
-                    if (c * W / G >= (c + 1) * W / G) continue;
-                }
-                merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, cb);
-                flags |= q[k].flags;
-            }
-        }
+        k2_merge_row(a, a.partials, a.rowunits, W, G, r, cb, st, flags);
         float H = kLn2 * (log2f(st.S) - st.T2 / st.S);
         if (H < 0.0f) H = 0.0f;                  // rounding below zero (NaN passes through)
         H = H + 0.0f;                            // -0 -> +0 so the key bits order correctly
@@ -606,6 +617,18 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const int A = st.ai;
         const int Y = m ? st.bi : -1;
         const unsigned long long hq = bad ? 0ull : (unsigned long long)__float2ull_rn(H * 1099511627776.0f);
+        unsigned long long hstat = hq;           // the entropy the stop rule sums
+        if (a.raw_partials) {
+            // EB_FLAG_STOP_RAW_ENTROPY: the entropy of the raw logits (T = 1), same fixed point
+            RowState sr = empty_state();
+            int rflags = 0;
+            k2_merge_row(a, a.raw_partials, a.raw_rowunits, Wr, Gr, r, kLog2e, sr, rflags);
+            float Hr = kLn2 * (log2f(sr.S) - sr.T2 / sr.S);
+            if (Hr < 0.0f) Hr = 0.0f;
+            if (!isfinite(Hr) || (rflags & kPartialNonfinite)) my_bad |= 1;
+            if (rflags & kPartialTimeout) my_bad |= 2;
+            hstat = my_bad ? 0ull : (unsigned long long)__float2ull_rn(Hr * 1099511627776.0f);
+        }
         Hq[p] = hq;
         Hf[p] = H;
         As[p] = A;
@@ -616,7 +639,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         a.sampled[r] = Y;
         // the stop statistics: every position, or the still-masked ones only
         if (m || !a.stop_masked_only) {
-            my_sum += hq;
+            my_sum += hstat;
             my_unstable |= (Pv[p] != A) ? 1 : 0;
         }
         if (m) {
@@ -995,10 +1018,12 @@ constexpr size_t align256c(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr size_t partial_bytes(long long rows) { return align256c((size_t)(rows + ebk::kMaxGrid) * sizeof(ebk::Partial)); }
 constexpr size_t prefix_bytes(long long rows) { return align256c((size_t)(rows + 1) * sizeof(uint32_t)); }
 constexpr size_t rowunit_bytes(long long rows) { return align256c((size_t)rows * sizeof(int2)); }
-constexpr size_t step_workspace_bytes(long long rows)
+constexpr size_t pass_workspace_bytes(long long rows)
 {
     return partial_bytes(rows) + prefix_bytes(rows) + rowunit_bytes(rows);
 }
+// Two copies: the step's row statistics, and the raw-logit pass of EB_FLAG_STOP_RAW_ENTROPY.
+constexpr size_t step_workspace_bytes(long long rows) { return 2 * pass_workspace_bytes(rows); }
 
 struct StepBuffers {
     uint8_t *mask;
@@ -1022,7 +1047,8 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
                        size_t ws_needed)
 {
     if (!params) return fail(EB_ERR_INVALID, "params is NULL");
-    if ((params->flags & ~(uint32_t)(EB_FLAG_DIAG_STALL | EB_FLAG_STOP_MASKED_ONLY | EB_FLAG_FINALIZE_SAMPLED)) != 0)
+    if ((params->flags & ~(uint32_t)(EB_FLAG_DIAG_STALL | EB_FLAG_STOP_MASKED_ONLY | EB_FLAG_FINALIZE_SAMPLED |
+                                     EB_FLAG_STOP_RAW_ENTROPY)) != 0)
         return fail(EB_ERR_INVALID, "params->flags has unknown bits 0x%x", params->flags);
     if (params->max_steps < 1) return fail(EB_ERR_INVALID, "max_steps must be >= 1");
     if (!(params->t_start > 0.0f) || !(params->t_end > 0.0f) || !std::isfinite(params->t_start) ||
@@ -1051,10 +1077,18 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
 }
 
 // Enqueues the selection kernel over the partial states of this step.
+struct RawPass {                 // partial states of the raw-logit pass, or all null
+    const ebk::Partial *partials = nullptr;
+    const uint32_t *prefix = nullptr;
+    const int2 *rowunits = nullptr;
+    int G = 0, weighted = 0;
+};
+
 eb_status launch_select(const eb_params *params, int B, int L, int step, float c, const StepBuffers &sb,
                         const ebk::Partial *partials, const uint32_t *prefix, const int2 *rowunits,
                         long long nvec_row,
-                        int rows, int G, int weighted, int k3_g, cudaStream_t stream)
+                        int rows, int G, int weighted, int k3_g, cudaStream_t stream,
+                        const RawPass &raw = RawPass())
 {
     ebk::K2Args a2;
     a2.partials = partials;
@@ -1087,6 +1121,11 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     a2.stop_entropy = (double)params->stop_entropy;
     a2.canvas_step = sb.canvas_step;
     a2.canvas_c = sb.canvas_c;
+    a2.raw_partials = raw.partials;
+    a2.raw_prefix = raw.prefix;
+    a2.raw_rowunits = raw.rowunits;
+    a2.raw_G = raw.G;
+    a2.raw_weighted = raw.weighted;
     a2.stop_masked_only = (params->flags & EB_FLAG_STOP_MASKED_ONLY) ? 1 : 0;
     a2.finalize_sampled = (params->flags & EB_FLAG_FINALIZE_SAMPLED) ? 1 : 0;
     a2.k3_g = k3_g;
@@ -1110,6 +1149,32 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
 }
 
 // Enqueues k1 + k2 for one step.  Arguments were validated by the caller.
+// One row-statistics launch of element kind `kind` over G partition units.
+eb_status launch_k1(int kind, int G, const ebk::K1Args &a1, cudaStream_t stream)
+{
+    switch (kind) {
+    // G counts warps (partition units); whole CTAs of kDirectWarps warps, the tail ones idle
+    case ebk::kF32Vec:
+        ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
+        break;
+    case ebk::kBF16Vec:
+        ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
+        break;
+    case ebk::kFP8Vec:
+        ebk::k1_rowstats_direct<ebk::kFP8Vec, ebk::kFP8U>
+            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
+        break;
+    case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    case ebk::kBF16Scalar: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    default: ebk::k1_rowstats_scalar<ebk::kFP8Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+    return EB_OK;
+}
+
 eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dtype,
                       const void *d_logits, int step, float T, const StepBuffers &sb,
                       void *d_ws, cudaStream_t stream)
@@ -1157,35 +1222,42 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a1.canvas_id = sb.canvas_id;
     a1.canvas_c = sb.canvas_c;
     a1.canvas_invT = sb.canvas_invT;
+    a1.raw = 0;
+    // EB_FLAG_STOP_RAW_ENTROPY: first a pass at T = 1 with every row unmasked (no sampling)
+    // into the second workspace copy; the selection kernel sums its entropies for the stop rule
+    RawPass raw;
+    if (params->flags & EB_FLAG_STOP_RAW_ENTROPY) {
+        ebk::K1Args ar = a1;
+        char *wr = ws + pass_workspace_bytes(rows);
+        ar.partials = reinterpret_cast<ebk::Partial *>(wr);
+        ar.prefix_out = reinterpret_cast<uint32_t *>(wr + partial_bytes(rows));
+        ar.rowunits = reinterpret_cast<int2 *>(wr + partial_bytes(rows) + prefix_bytes(rows));
+        ar.c = ebk::kLog2e;
+        ar.invT = 1.0f;
+        ar.canvas_step = nullptr;
+        ar.canvas_id = nullptr;
+        ar.canvas_c = nullptr;
+        ar.canvas_invT = nullptr;
+        ar.raw = 1;
+        st = launch_k1(kind, G, ar, stream);
+        if (st != EB_OK) return st;
+        raw.partials = ar.partials;
+        raw.prefix = ar.prefix_out;
+        raw.rowunits = ar.rowunits;
+        raw.G = G;
+        raw.weighted = ar.weighted;
+    }
     cudaEvent_t prof_begin = g_profile_begin, prof_end = g_profile_end;
     g_profile_begin = g_profile_end = nullptr;
     if (prof_begin && record_profile_event(prof_begin, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
-    switch (kind) {
-    // G counts warps (partition units); whole CTAs of kDirectWarps warps, the tail ones idle
-    case ebk::kF32Vec:
-        ebk::k1_rowstats_direct<ebk::kF32Vec, ebk::kDirectU>
-            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
-        break;
-    case ebk::kBF16Vec:
-        ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>
-            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
-        break;
-    case ebk::kFP8Vec:
-        ebk::k1_rowstats_direct<ebk::kFP8Vec, ebk::kFP8U>
-            <<<(G + ebk::kDirectWarps - 1) / ebk::kDirectWarps, ebk::kDirectThreads, ebk::kDirectStageBytes, stream>>>(a1);
-        break;
-    case ebk::kF32Scalar: ebk::k1_rowstats_scalar<ebk::kF32Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
-    case ebk::kBF16Scalar: ebk::k1_rowstats_scalar<ebk::kBF16Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
-    default: ebk::k1_rowstats_scalar<ebk::kFP8Scalar><<<G, ebk::kConsumers, 0, stream>>>(a1); break;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(EB_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+    st = launch_k1(kind, G, a1, stream);
+    if (st != EB_OK) return st;
     if (prof_end && record_profile_event(prof_end, stream) != cudaSuccess)
         return fail(EB_ERR_CUDA, "cudaEventRecord failed");
 
     return launch_select(params, B, L, step, a1.c, sb, partials, prefix, rowunits, nvec_row, (int)rows, G,
-                         a1.weighted, 0, stream);
+                         a1.weighted, 0, stream, raw);
 }
 
 // Enqueues the fused unembedding kernel (+ the selection kernel unless logits_out is given).
@@ -1195,6 +1267,8 @@ eb_status launch_unembed(const eb_params *params, int B, int L, int K, int V, co
                          float *logits_out, cudaStream_t stream)
 {
     namespace k3 = ebk::k3;
+    if (params && (params->flags & EB_FLAG_STOP_RAW_ENTROPY))
+        return fail(EB_ERR_UNSUPPORTED, "EB_FLAG_STOP_RAW_ENTROPY needs the logits twice; the fused path never stores them");
     int nsm = 0;
     eb_status st = unembed_geometry(&nsm);
     if (st != EB_OK) return st;

@@ -21,9 +21,9 @@
  *      masked take A (step cap).
  * The pages give no selection formula; the rule of item 4 is the one this library
  * implements (the longest sorted prefix whose sum minus its maximum stays within the
- * bound).  Items 3 and 5 state the default readings of two open points; EB_FLAG_* bits of
- * eb_params.flags select the alternatives (stop statistics over the masked positions only,
- * sampled-token finalisation).
+ * bound).  Items 3 and 5 state the default readings of open points; EB_FLAG_* bits of
+ * eb_params.flags select the alternatives (stop statistics over the masked positions only or
+ * of the raw logits, sampled-token finalisation).
  *
  * Conventions shared by every entry point:
  *   - every d_* pointer is DEVICE memory owned by the caller; the library allocates
@@ -89,9 +89,14 @@ typedef struct {
  *   EB_FLAG_STOP_MASKED_ONLY: the stop statistics run over the positions still masked at the
  *     start of the step (mean_entropy then reports that mean);
  *   EB_FLAG_FINALIZE_SAMPLED: positions finalised at an adaptive stop or at the step cap take
- *     their sampled token instead of the argmax. */
+ *     their sampled token instead of the argmax;
+ *   EB_FLAG_STOP_RAW_ENTROPY: the stop rule's mean uses the entropy of the raw logits (T = 1)
+ *     instead of the shaped ones (selection still uses the shaped entropy; mean_entropy then
+ *     reports the raw mean).  It costs a second, sampling-free pass over the logits; the fused
+ *     entry point refuses it (EB_ERR_UNSUPPORTED), as its logits are never stored. */
 #define EB_FLAG_STOP_MASKED_ONLY 2u
 #define EB_FLAG_FINALIZE_SAMPLED 4u
+#define EB_FLAG_STOP_RAW_ENTROPY 8u
 
 /* Diagnostic bit of eb_params.flags.  The fused unembedding kernel of eb_unembed_sample then
  * withholds its first operand load and lets each device wait poll only a few thousand times.
@@ -157,8 +162,8 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
  *   - a latency-critical loop where the implicit synchronisation of an allocation is not
  *     acceptable.
  * The per-row partial states live instead in one fixed array of device memory inside this
- * library, sized for at most EB_NOALLOC_MAX_ROWS canvas positions (B * L).  That is 622,848
- * bytes, and every device that loads the library holds them until the process exits.
+ * library, sized for at most EB_NOALLOC_MAX_ROWS canvas positions (B * L).  That is
+ * 1,245,696 bytes, and every device that loads the library holds them until the process exits.
  *
  * Arguments, results and errors are those of eb_sampler_step, with the workspace supplied by
  * the library.  B * L above EB_NOALLOC_MAX_ROWS returns EB_ERR_UNSUPPORTED and launches

@@ -184,12 +184,13 @@ class Params:
     entropy_bound: float = 0.1
     stop_entropy: float = 0.005
     seed: int = 0
-    flags: int = 0            # reading variants: STOP_MASKED_ONLY, FINALIZE_SAMPLED
+    flags: int = 0            # reading variants: STOP_MASKED_ONLY, FINALIZE_SAMPLED, STOP_RAW_ENTROPY
 
 
 # Reading variants of the stop / finalisation rules (Params.flags bits)
 STOP_MASKED_ONLY = 2          # stop statistics over the still-masked positions only
 FINALIZE_SAMPLED = 4          # positions finalised at stop / cap take the sampled token
+STOP_RAW_ENTROPY = 8          # stop statistics on the entropy of the raw logits (T = 1)
 
 
 @dataclass

@@ -268,9 +268,12 @@ int eb_oracle_select(int L, const double *H, const uint8_t *mask, double bound,
  *   STOP_MASKED_ONLY  the stop rule's mean entropy and its argmax-stability test run over
  *                     the positions still masked at the start of the step, instead of all L;
  *   FINALIZE_SAMPLED  on adaptive stop and at the step cap the positions still masked take
- *                     their sampled token Y instead of the argmax A. */
+ *                     their sampled token Y instead of the argmax A;
+ *   STOP_RAW_ENTROPY  the stop rule's mean entropy is that of the raw logits (T = 1) instead
+ *                     of the shaped ones; selection keeps the shaped entropy. */
 #define ORACLE_FLAG_STOP_MASKED_ONLY 2u
 #define ORACLE_FLAG_FINALIZE_SAMPLED 4u
+#define ORACLE_FLAG_STOP_RAW_ENTROPY 8u
 
 /* One full EB sampler step over B canvases of L positions (logits [B, L, V]).
  *
@@ -302,6 +305,9 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
     size_t esize = dtype == 0 ? 4 : (dtype == 1 ? 2 : (dtype == 3 ? 1 : 8));
     int64_t rows = (int64_t)B * L;
 
+    /* the raw-logit entropies of STOP_RAW_ENTROPY: the same row at T = 1, no sampling */
+    double *Hraw = (flags & ORACLE_FLAG_STOP_RAW_ENTROPY) ? (double *)malloc((size_t)rows * sizeof(double)) : NULL;
+
     #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < rows; ++r) {
         int b = (int)(r / L), p = (int)(r % L);
@@ -313,6 +319,11 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
         const char *row = (const char *)logits + (size_t)r * (size_t)V * esize;
         eb_oracle_row(row, dtype, V, T, mask[r], seed, canvas_ids ? canvas_ids[b] : b, p, step,
                       &H[r], &A[r], &Y[r], &gap[r]);
+        if (Hraw) {
+            int32_t a2, y2;
+            double g2;
+            eb_oracle_row(row, dtype, V, 1.0, 0, seed, b, p, step, &Hraw[r], &a2, &y2, &g2);
+        }
     }
 
     for (int b = 0; b < B; ++b) {
@@ -330,7 +341,7 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
         int stable = 1;
         for (int p = 0; p < L; ++p) {
             if (masked_only && !mask[base + p]) continue;
-            sumH += H[base + p];
+            sumH += Hraw ? Hraw[base + p] : H[base + p];
             ++nstat;
             if (A[base + p] != prev_argmax[base + p]) stable = 0;
         }
@@ -384,6 +395,7 @@ void eb_oracle_step(int B, int L, int64_t V, int dtype, const void *logits,
         for (int p = 0; p < L; ++p) prev_argmax[base + p] = A[base + p];
         if (committed) committed[b] = count;
     }
+    free(Hraw);
 }
 
 /* Number of OpenMP threads the oracle's row loop uses. */

@@ -96,7 +96,7 @@ def test_invalid_arguments_rejected_before_launch(libs, kw, status):
 
 
 def test_invalid_params_rejected(libs):
-    for field, value in (("max_steps", 0), ("t_start", 0.0), ("t_end", -1.0), ("flags", 8),
+    for field, value in (("max_steps", 0), ("t_start", 0.0), ("t_end", -1.0), ("flags", 16),
                          ("flags", 0x80000001), ("entropy_bound", float("inf"))):
         p = eb.eb_default_params()
         setattr(p, field, value)

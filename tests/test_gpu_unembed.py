@@ -212,3 +212,14 @@ def test_unembed_stalled_load_times_out_and_context_survives():
     assert rep.max_h_err < H_TOL
     assert rep.canvas_ties <= 1
 
+
+
+def test_unembed_refuses_the_raw_entropy_flag():
+    gp, _ = params_pair()
+    gp.flags = eb.EB_FLAG_STOP_RAW_ENTROPY
+    c = eb.Canvas(1, 16, 64, eb.EB_BF16)
+    h = torch.zeros((16, 16), dtype=torch.int16, device="cuda")
+    W = torch.zeros((16, 64), dtype=torch.int16, device="cuda")
+    with pytest.raises(eb.EbError) as ei:
+        c.unembed_step(gp, h, W, 16, 0, 0.8)
+    assert ei.value.status == eb.EB_ERR_UNSUPPORTED

@@ -464,3 +464,21 @@ def test_e4m3_row_equals_its_decoded_values():
     a = oracle.row(codes, 0.8, True, 3, 0, 7, 2)
     b = oracle.row(e4m3_bits_to_f32(codes).astype(np.float64), 0.8, True, 3, 0, 7, 2)
     assert a[0] == b[0] and a[1] == b[1] and a[2] == b[2]
+
+
+def test_raw_entropy_stop_statistic():
+    """STOP_RAW_ENTROPY: the stop rule averages the entropy of the raw logits (T = 1).  A peak of
+    9 over 15 zeros has a raw entropy of about 0.019 nats but a shaped one (T = 0.79 at step 1)
+    of about 0.002, so the default stops and the variant does not; selection is unchanged."""
+    B, L, V = 1, 8, 16
+    x = _peaked(B, L, V, [[p + 1 for p in range(L)]], height=9.0)
+    raw_h = oracle.row(x[0, 0], 1.0, False)[0]
+    shaped_h = oracle.row(x[0, 0], oracle.temperature(1), False)[0]
+    assert shaped_h < 0.005 < raw_h
+    for flags, expect in ((0, oracle.ADAPTIVE), (oracle.STOP_RAW_ENTROPY, oracle.RUNNING)):
+        st = oracle.State.fresh(B, L)
+        st.prev_argmax[:] = [[p + 1 for p in range(L)]]
+        r = oracle.step(x, st, 1, oracle.Params(flags=flags, entropy_bound=-1.0))
+        assert st.status[0] == expect
+        assert r.mean_entropy[0] == pytest.approx(raw_h if flags else shaped_h, rel=1e-12)
+        assert r.H[0, 0] == pytest.approx(shaped_h, rel=1e-12)

@@ -514,14 +514,14 @@ def test_finalize_sampled_parity_at_stop_and_cap():
 
 
 def test_raw_entropy_stop_parity():
-    """EB_FLAG_STOP_RAW_ENTROPY: the stop statistic from a second pass at T = 1.  Peaks of 9
-    stop the default (shaped entropy ~0.002) but not the variant (raw ~0.019); both match the
-    oracle, and a lockstep loop with the flag matches it step by step."""
+    """EB_FLAG_STOP_RAW_ENTROPY: the stop statistic from a second pass at T = 1.  Peaks of 12
+    over 511 zeros stop the default (shaped entropy ~0.002) but not the variant (raw ~0.041);
+    both match the oracle, and a lockstep loop with the flag matches it step by step."""
     B, L, V = 2, 64, 512
     x = np.zeros((B, L, V), np.float32)
     peak = (np.arange(L) * 5 + 1) % V
     for b in range(B):
-        x[b, np.arange(L), peak] = 9.0
+        x[b, np.arange(L), peak] = 12.0
     prev = np.broadcast_to(peak, (B, L)).astype(np.int32)
     g, res, ost, _ = _variant_step(x, 0, prev=prev, entropy_bound=-1.0)
     assert (g["status"] == eb.EB_STOP_ADAPTIVE).all() and (ost.status == oracle.ADAPTIVE).all()

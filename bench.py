@@ -44,12 +44,22 @@ KERNEL_SRCS = [os.path.join(ROOT, "canvas_sampler_step_b300", "csrc", f)
                for f in ("eb_sampler.cu", "eb_kernels.cuh")]
 
 
+def _strip_comments(text: str) -> str:
+    """C++ source without // and /* */ comments or trailing blanks (string literals in these
+    sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the row-statistics kernel's sources."""
+    """First 16 hex digits of the SHA-256 of the row-statistics kernel's sources, comments
+    left out, so that a comment edit does not void a recorded traffic figure."""
     h = hashlib.sha256()
     for f in KERNEL_SRCS:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

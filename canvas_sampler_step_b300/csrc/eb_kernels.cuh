@@ -9,28 +9,30 @@
 //     which also draw Gumbel noise, w_unmasked otherwise; rows of halted canvases weigh 0).
 //     The prefix sums P of the weights are cut into G equal ranges, one per warp (16 warps per
 //     CTA, one CTA per SM), so warps finish together even though masked rows cost more
-//     instructions per byte, and halted canvases cost nothing.  Warp g writes one partial
-//     state for every row its range touches to slot (row + g) of the workspace (the (row,
-//     warp) pairs form a staircase, so row + g is unique).
-//   * Data movement.  Each lane copies the 16-byte vectors it will consume, two per batch, with
-//     cp.async (L2 evict-first, no L1) into its own shared-memory slots four batches ahead of
-//     use, and waits only for its own oldest group; warps read their slots conflict-free and
-//     run whole batches without bounds checks.  (A TMA bulk-copy ring with a producer warp
-//     measured slower on this workload: 81.7 us against 78 us, its consumers idling on the
-//     ring's barriers; register double buffering had too little in flight: 47.6 us against
-//     41.9 us on unmasked rows.)
+//     instructions per byte, and halted canvases cost nothing.  Unit u runs on CTA u mod G/16,
+//     so every SM mixes masked and unmasked work.  Unit g writes one partial state for every
+//     row its range touches to slot (row + g) of the workspace (the (row, unit) pairs form a
+//     staircase, so row + g is unique).
+//   * Data movement.  Each lane copies the 16-byte vectors it will consume (two per batch;
+//     one for e4m3, whose vector holds 16 logits) with cp.async (L2 evict-first, no L1) into
+//     its own shared-memory slots four batches ahead of use, and waits only for its own
+//     oldest group; the slot offset and the global pointer advance by constants.  Whole
+//     batches run without bounds checks, the ragged tail with guarded plain loads.  (A TMA
+//     bulk-copy ring with a producer warp measured slower on this workload, its consumers
+//     idling on the ring's barriers; register double buffering had too little in flight.)
 //   * Per element: t = x * log2(e)/T - xm * log2(e)/T, e = 2^t (MUFU), S += e, T2 += t e,
-//     with xm the running maximum of the thread's raw logits (first index kept for the
-//     argmax); the FMAs and adds run on packed f32x2 pairs.  H = ln 2 (log2 S - T2 / S)
-//     after merging.  A new running maximum is handled behind a warp vote so that the rare
-//     rescale stays a branch.
+//     with xm the warp's running maximum of the raw logits (first index kept for the argmax);
+//     the FMAs and adds run on packed f32x2 pairs.  H = ln 2 (log2 S - T2 / S) after merging.
+//     A batch takes one new-maximum vote, so the rare rescale stays a branch.
 //   * Gumbel-max for masked rows: with u from a Philox4x32-10 word and E = -ln u, the sample
 //     maximises z - ln E.  Since E >= 1 - u, an entry can beat the best score so far only if
-//     1 - u < 2^t K, K = 2^(xm log2e / T - best log2e); that test is one LOP3, one FFMA and
-//     one predicate-or per entry.  Entries that pass it (a handful per warp and row) take the
-//     exact score z - logf(-log1pf(-(1 - u))) in an out-of-line function; the warp shares its
+//     1 - u < 2^t K, K = 2^(xm log2e / T - best log2e); one candidate vote per batch.  Entries
+//     that pass (a handful per warp and row) take the exact score z - logf(-log1pf(-(1 - u)))
+//     in an out-of-line function, handed the Philox words already drawn; the warp shares its
 //     best score when it moves.
-// k2_select (one CTA per canvas) merges each row's partials in ascending CTA order
+//   * Optional per-canvas step, temperature and Philox canvas id (the block driver), and a
+//     sampling-free raw mode at T = 1 (the raw-logit entropy of the stop rule's variant).
+// k2_select (one CTA per canvas) merges each row's partials in ascending unit order
 // (deterministic), runs the stop test, the entropy-bounded selection and the commit /
 // re-mask / finalisation.  Sums of entropies are exact 64-bit fixed point (2^-40 nats).
 #pragma once

@@ -58,3 +58,14 @@ def test_clock_summary_reads_samples_and_reasons():
     assert s["sm_max_mhz"] == 2032.0
     assert s["reasons"] == ["sw_power_cap"]
     assert s["samples"] == 3 and s["power_w_max"] == pytest.approx(1090.9)
+
+
+def test_source_hash_ignores_comments(tmp_path, monkeypatch):
+    src = tmp_path / "k.cuh"
+    src.write_text("// kernel\nint f(int x) { return x + 1; }  // add one\n/* block */\n")
+    monkeypatch.setattr(bench, "KERNEL_SRCS", [str(src)])
+    h = bench.kernel_source_hash()
+    src.write_text("// the kernel, described anew\n\nint f(int x) { return x + 1; }\n")
+    assert bench.kernel_source_hash() == h
+    src.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_source_hash() != h

@@ -509,20 +509,33 @@ def run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, wor
 # ------------------------------------------------------------------ CPU oracle legs
 
 def cpu_baseline():
-    """The oracle, as it stands, on one full step of the workload (seed 0: 256 rows x
-    262144 bf16, 128 masked) with all its OpenMP threads on the host cores."""
+    """The oracle, as it stands, on full steps of the workload (seed 0: 256 rows x 262144
+    bf16, 128 masked): the median of three steps with all its OpenMP threads on the host
+    cores, and one step on a single thread."""
     import eb_synth
     import oracle
     cfg = eb_synth.cfg1(0)
     x = cfg.logits(0)
     mask = eb_synth.cfg1_mask(0)
-    st = oracle.State.fresh(B, L, mask)
-    t0 = time.perf_counter()
-    oracle.step(x, st, 0, oracle.Params(seed=0), temperature=float(np.float32(TEMPERATURE)))
-    dt = time.perf_counter() - t0
-    return {"value": 1.0 / dt, "unit": "steps/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "one full step of seed 0 (256 rows x 262144 bf16, 128 masked), all rows "
-                      f"and the selection; {dt:.2f} s wall"}
+
+    def one():
+        st = oracle.State.fresh(B, L, mask)
+        t0 = time.perf_counter()
+        oracle.step(x, st, 0, oracle.Params(seed=0), temperature=float(np.float32(TEMPERATURE)))
+        return time.perf_counter() - t0
+
+    cores = oracle.num_threads()
+    dt = statistics.median(one() for _ in range(3))
+    oracle.set_num_threads(1)
+    try:
+        dt1 = one()
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": 1.0 / dt, "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "one_thread_value": 1.0 / dt1,
+            "sample": "full steps of seed 0 (256 rows x 262144 bf16, 128 masked), all rows and the "
+                      f"selection: median of 3 on {cores} threads ({dt:.2f} s wall each), "
+                      f"1 on one thread ({dt1:.2f} s)"}
 
 
 def run_reference(args, rank, world, local):

@@ -108,3 +108,27 @@ def test_slot_generator_matches_the_batch_generator():
             assert (got[b] == 123.0).all()
         else:
             assert np.array_equal(got[b], cfg.logits(s)[k])
+
+
+def test_blocks_on_e4m3_logits_equal_the_batch_loop():
+    """The block driver on e4m3 logits (16 per vector, per-slot steps): block k again equals
+    canvas k of the plain loop over all blocks at once."""
+    import dataclasses
+    cfg = dataclasses.replace(_cfg(), dtype="fp8")
+    gp, _ = params_pair(seed=5)
+    recipe = synth_dev.Recipe.of(cfg)
+    logits = torch.empty((4, L, V), dtype=torch.uint8, device="cuda")
+    ws_bytes = eb.eb_blocks_workspace_bytes(4, L, V, eb.EB_FP8_E4M3)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    toks = torch.full((N, L), -7, dtype=torch.int32, device="cuda")
+    steps = torch.zeros(N, dtype=torch.int32, device="cuda")
+    status = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    eb.eb_sample_blocks(gp, 4, L, V, eb.EB_FP8_E4M3, synth_dev.block_callback_address(),
+                        ctypes.addressof(recipe), logits, N, toks, steps, status, ws, ws_bytes, 4)
+    c = eb.Canvas(N, L, V, eb.EB_FP8_E4M3, max_steps=gp.max_steps)
+    buf = torch.empty((N, L, V), dtype=torch.uint8, device="cuda")
+    c.run(gp, synth_dev.callback_address(), ctypes.addressof(recipe), buf)
+    torch.cuda.synchronize()
+    assert np.array_equal(status.cpu().numpy(), c.status.cpu().numpy())
+    assert np.array_equal(steps.cpu().numpy(), c.steps_taken.cpu().numpy())
+    assert np.array_equal(toks.cpu().numpy(), c.tokens.cpu().numpy())

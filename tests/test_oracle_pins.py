@@ -482,3 +482,18 @@ def test_raw_entropy_stop_statistic():
         assert st.status[0] == expect
         assert r.mean_entropy[0] == pytest.approx(raw_h if flags else shaped_h, rel=1e-12)
         assert r.H[0, 0] == pytest.approx(shaped_h, rel=1e-12)
+
+
+def test_raw_and_masked_only_statistics_combine():
+    """STOP_RAW_ENTROPY | STOP_MASKED_ONLY: the mean of the raw-logit entropies over the
+    positions still masked."""
+    B, L, V = 1, 8, 16
+    x = _peaked(B, L, V, [[p + 1 for p in range(L)]], height=9.0)
+    x[0, :4, :] = 0.0                                        # committed rows: uniform
+    st = oracle.State.fresh(B, L)
+    st.mask[0, :4] = 0
+    st.tokens[0, :4] = 3
+    r = oracle.step(x, st, 1, oracle.Params(flags=oracle.STOP_RAW_ENTROPY | oracle.STOP_MASKED_ONLY,
+                                            entropy_bound=-1.0))
+    raw_h = oracle.row(x[0, 4], 1.0, False)[0]
+    assert r.mean_entropy[0] == pytest.approx(raw_h, rel=1e-12)

@@ -497,3 +497,21 @@ def test_raw_and_masked_only_statistics_combine():
                                             entropy_bound=-1.0))
     raw_h = oracle.row(x[0, 4], 1.0, False)[0]
     assert r.mean_entropy[0] == pytest.approx(raw_h, rel=1e-12)
+
+
+def test_entropy_against_50_digit_arithmetic():
+    """H = ln S - T'/S of the shaped logits, against the definition -sum p ln p evaluated with
+    50 significant digits (mpmath), on rows with a wide logit range, at two temperatures."""
+    import mpmath
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(21)
+    for T in (0.8, 0.4):
+        for scale in (1.0, 12.0):
+            x = (rng.standard_normal(257) * scale).astype(np.float32)
+            H = oracle.row(x, T, False)[0]
+            z = [mpmath.mpf(float(v)) / mpmath.mpf(T) for v in x]
+            m = max(z)
+            w = [mpmath.e ** (zi - m) for zi in z]
+            s = mpmath.fsum(w)
+            ref = -mpmath.fsum((wi / s) * mpmath.log(wi / s) for wi in w)
+            assert abs(H - float(ref)) <= 1e-12 * max(1.0, float(ref)), (T, scale, H, float(ref))

@@ -1076,7 +1076,6 @@ eb_status check_common(const eb_params *params, int B, int L, int V, eb_dtype dt
     return EB_OK;
 }
 
-// Enqueues the selection kernel over the partial states of this step.
 struct RawPass {                 // partial states of the raw-logit pass, or all null
     const ebk::Partial *partials = nullptr;
     const uint32_t *prefix = nullptr;
@@ -1084,6 +1083,8 @@ struct RawPass {                 // partial states of the raw-logit pass, or all
     int G = 0, weighted = 0;
 };
 
+// Enqueues the selection kernel over the partial states of this step (and of the raw-logit
+// pass, when given) as a programmatic dependent of the row-statistics grid.
 eb_status launch_select(const eb_params *params, int B, int L, int step, float c, const StepBuffers &sb,
                         const ebk::Partial *partials, const uint32_t *prefix, const int2 *rowunits,
                         long long nvec_row,

@@ -14,6 +14,12 @@ of its canvas state so each step does the same work.
 Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs its own replica
 (the sampler has no cross-canvas exchange) and the value is all ranks' steps over the
 slowest rank's time.  ``--impl reference`` times the CPU oracle on the host cores instead.
+
+The headline line also carries, under "workloads", one record per other workload, each
+measured in the same run on the same GPU: the fused unembedding step (4 canvases and one),
+the full adaptive loop of one canvas and of the mixed batch of eight (steps to stop, tokens
+committed per step), the e4m3 single step and the block driver.  ``--workload NAME`` prints
+one of them as the line instead.
 """
 from __future__ import annotations
 
@@ -34,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "EB-sampler steps/s at B×256×262144 bf16; achieved HBM GB/s vs B300 peak"
 B, L, V = 1, 256, 262144
 NSEEDS = 10
-PROF_EVERY = 20                          # steps per timed row-statistics launch
+K1_SAMPLES = 60                          # row-statistics launches timed one by one
 BYTES_PER_STEP = B * L * V * 2           # algorithmic bytes: every logit read once
 TEMPERATURE = 0.8
 WORKLOAD = ("single EB sampler step: B=1 canvas, L=256 positions, V=262144 bf16 logits "
@@ -73,12 +79,15 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--logits", choices=("bf16", "fp8"), default="bf16",
                     help="element type of the single-step workload's logits (fp8: OCP e4m3)")
-    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "blocks"), default="single",
+    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "loop1", "blocks"),
+                    default="single",
                     help="single: the single-step workload (default, the headline line); fused: "
                          "the fused unembedding + sampler step (4 x 256 positions, K=2048); "
                          "fused1: the same for one canvas (256 positions); loop: the adaptive "
-                         "48-step loop over 8 canvases with the stand-in denoiser; blocks: the "
-                         "block driver, 64 blocks on 8 slots")
+                         "48-step loop over 8 canvases with the stand-in denoiser; loop1: the "
+                         "same for one canvas; blocks: the block driver, 64 blocks on 8 slots")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline only: leave out the per-workload records")
     return ap.parse_args(argv)
 
 
@@ -293,33 +302,62 @@ def state_ptrs(pool, i):
     return out
 
 
-def run_ours(args, rank, world, local):
-    import ctypes
+def k1_sample_times(lib, step_call, n, pool_restore, stream, torch):
+    """CUDA-event durations (ms) of n row-statistics launches, each bracketed by its own pair of
+    events on the launching stream (eb_set_profile_events); every launch is a whole step on a
+    fresh canvas state, restored before the first event.  One synchronisation at the end."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for b, e in evs:
+        b.record(stream)
+        e.record(stream)          # materialise the CUDA events
+    torch.cuda.synchronize()
+    for i, (b, e) in enumerate(evs):
+        pool_restore(i)
+        lib.eb_set_profile_events(b.cuda_event, e.cuda_event)
+        step_call(i)
+    torch.cuda.synchronize()
+    return [b.elapsed_time(e) for b, e in evs]
 
+
+def sample_stats(ms):
+    """median / p10 / p90 / mean of a list of durations (ms), and their count."""
+    a = np.sort(np.asarray(ms, dtype=np.float64))
+    return {"n": int(a.size), "median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "mean_ms": float(a.mean())}
+
+
+def single_step_setup(args, lk, device, W):
+    """Resident inputs of the single-step workload: NSEEDS rotating logit buffers, the initial
+    masks, a pool of W canvas states and the workspace."""
     import torch
 
     import canvas_sampler_step_b300 as eb
-    import eb_synth
     import eb_synth.device as synth_dev
-
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
-    eb.lib()
-    synth_dev.lib()
-    lib = eb.lib()
-    stream = torch.cuda.current_stream(device)
-    sp = stream.cuda_stream
-
-    # inputs resident in HBM before the timed region
-    lk = logits_kind(args, eb, torch)
     bufs = []
     for seed in range(NSEEDS):
         x = torch.empty((B, L, V), dtype=lk["torch"], device=device)
         synth_dev.logits(synth_dev.Recipe.of(lk["cfg"](seed)), 0, x)
         bufs.append(x)
     masks = workload_masks()
-    K, W = args.steps, args.warmup
+    ws_bytes = eb.eb_workspace_bytes(B, L, V, lk["eb"])
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    return bufs, masks, ws, ws_bytes
+
+
+def run_single(args, lk, device, local, dist, world, timed=True):
+    """The single-step workload (bf16 or e4m3 logits): the timed region is `steps` steps as
+    replays of a CUDA graph of N steps (plus one canvas-state restore per replay), then
+    K1_SAMPLES row-statistics launches timed one by one.  Returns the measurement dict."""
+    import ctypes
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    lib = eb.lib()
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+    K, W = args.steps, max(args.warmup, 3)
+    bufs, masks, ws, ws_bytes = single_step_setup(args, lk, device, W)
     # the timed steps run as replays of a CUDA graph of N steps (N divides K), so the host's
     # per-call cost stays out of the device time; each replay first restores its N canvas
     # states from a pristine copy, so every step does the workload's work
@@ -330,8 +368,6 @@ def run_ours(args, rank, world, local):
     ptrs = [state_ptrs(pool, i) for i in range(N)]
     wpool = state_pool(W, masks, device)
     wptrs = [state_ptrs(wpool, i) for i in range(W)]
-    ws_bytes = eb.eb_workspace_bytes(B, L, V, lk["eb"])
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     params = eb.eb_default_params(seed=0)
     pref = ctypes.byref(params)
     buf_ptrs = [b.data_ptr() for b in bufs]
@@ -339,7 +375,7 @@ def run_ours(args, rank, world, local):
     step_fn = lib.eb_sampler_step
 
     def one(i, sptrs, stream_ptr):
-        st = step_fn(pref, B, L, V, lk["eb"], buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *sptrs[i],
+        st = step_fn(pref, B, L, V, lk["eb"], buf_ptrs[i % NSEEDS], 0, TEMPERATURE, *sptrs[i % len(sptrs)],
                      wsp, ws_bytes, stream_ptr)
         if st != 0:
             raise eb.EbError(st, lib.eb_last_error().decode())
@@ -347,20 +383,6 @@ def run_ours(args, rank, world, local):
     for i in range(W):
         one(i, wptrs, sp)
     torch.cuda.synchronize()
-
-    # the row-statistics kernel is timed by CUDA events recorded around it on one step in
-    # PROF_EVERY: an event node in the graph costs about 8 us of device time per step, which
-    # would otherwise be charged to every step
-    prof_steps = list(range(0, N, PROF_EVERY))
-    k1b = [torch.cuda.Event(enable_timing=True) for _ in prof_steps]
-    k1e = [torch.cuda.Event(enable_timing=True) for _ in prof_steps]
-    for e in k1b + k1e:
-        e.record(stream)          # materialise the CUDA events before capture
-    torch.cuda.synchronize()
-    evb = {j: e.cuda_event for j, e in zip(prof_steps, k1b)}
-    eve = {j: e.cuda_event for j, e in zip(prof_steps, k1e)}
-    set_prof = lib.eb_set_profile_events
-
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device)
     with torch.cuda.stream(cap):
@@ -369,8 +391,6 @@ def run_ours(args, rank, world, local):
             pool[k].copy_(pristine[k])
         csp = torch.cuda.current_stream(device).cuda_stream
         for j in range(N):
-            if j in evb:
-                set_prof(evb[j], eve[j])
             one(j, ptrs, csp)
         graph.capture_end()
     torch.cuda.synchronize()
@@ -378,7 +398,6 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-
     barrier(dist, local)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -389,30 +408,57 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
     barrier(dist, local)
     elapsed = start.elapsed_time(end) / 1e3
-    k1_ms = [b.elapsed_time(e) for b, e in zip(k1b, k1e)]     # sampled launches of the last replay
     value, slowest = aggregate(K, elapsed, world, dist, local)
-
     # every timed step did the workload's work: running canvas, one position committed
     st = pool["status"].cpu().numpy()
     com = pool["committed"].cpu().numpy()
     if not ((st == 0).all() and (com >= 1).all()):
         raise RuntimeError("timed steps did not run the expected workload")
 
-    k1_avg_s = statistics.mean(k1_ms) / 1e3
+    # the row-statistics kernel alone: K1_SAMPLES launches, each timed by its own events
+    spool = state_pool(NSEEDS, masks, device)
+    spristine = {k: v.clone() for k, v in spool.items()}
+    sptrs = [state_ptrs(spool, i) for i in range(NSEEDS)]
+
+    def restore(i):
+        j = i % NSEEDS
+        for k in spool:
+            spool[k][j].copy_(spristine[k][j])
+
+    k1_ms = k1_sample_times(lib, lambda i: one(i, sptrs, sp), K1_SAMPLES, restore, stream, torch)
+    k1 = sample_stats(k1_ms)
+    return {"value": value, "elapsed": elapsed, "slowest": slowest, "K": K, "W": W, "N": N, "R": R,
+            "k1": k1, "clocks": clocks.summary(), "bufs": bufs, "masks": masks, "params": params,
+            "stream": stream}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth.device as synth_dev
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    lib = eb.lib()
+    synth_dev.lib()
+    lk = logits_kind(args, eb, torch)
+    m = run_single(args, lk, device, local, dist, world)
+    K, W = m["K"], m["W"]
     peak, peak_kind = measured_peaks()
-    achieved = lk["bytes"] / k1_avg_s / 1e9
+    k1 = m["k1"]
+    achieved = lk["bytes"] / (k1["median_ms"] / 1e3) / 1e9
     traffic = recorded_traffic() if lk["name"] == "bf16" else None
-
-    e2e = run_e2e(args, eb, lib, bufs, masks, params, device, stream, dist, local, world, lk)
-
+    e2e = run_e2e(args, eb, lib, m["bufs"], m["masks"], m["params"], device, m["stream"], dist, local, world, lk)
     out = {
         "metric": lk["metric"],
-        "value": value,
+        "value": m["value"],
         "unit": "steps/s",
         "n_gpus": world,
         "steps": K,
         "warmup": W,
-        "ms_per_step": slowest * 1e3 / K,
+        "ms_per_step": m["slowest"] * 1e3 / K,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -422,12 +468,13 @@ def run_ours(args, rank, world, local):
             "workload": lk["workload"],
             "B": B, "L": L, "V": V, "logits_dtype": lk["name"], "masked": 128, "temperature": TEMPERATURE,
             "l2": f"10 rotating {lk['bytes'] >> 20} MiB logit buffers ({10 * lk['bytes'] / 2**30:.3g} GiB > 126 MB L2)",
-            "launch": f"CUDA graph of {N} steps (+ one canvas-state restore) replayed {R} times; "
-                      f"row-statistics kernel timed by events on {len(prof_steps)} steps per replay",
+            "launch": f"CUDA graph of {m['N']} steps (+ one canvas-state restore) replayed {m['R']} times; "
+                      f"row-statistics kernel timed separately over {K1_SAMPLES} launches, each between its "
+                      "own CUDA events",
             "parallelism": f"replicas x{world}",
         },
-        "hbm_gbs_step": lk["bytes"] * K / elapsed / 1e9,
-        "positions_per_s": value * B * L,
+        "hbm_gbs_step": lk["bytes"] * K / m["elapsed"] / 1e9,
+        "positions_per_s": m["value"] * B * L,
         "roofline": {
             "bound": "hbm",
             "kernel": f"k1_rowstats<{lk['name']}>",
@@ -437,14 +484,23 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "k1_ms_mean": statistics.mean(k1_ms),
-            "k1_ms_median": statistics.median(k1_ms),
+            "traffic_source": (f"recorded: ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, from "
+                               f"profiles/k1_rowstats_bf16_single_step.md, taken on kernel sources with hash "
+                               f"{kernel_source_hash()} (the sources of this run)") if traffic is not None
+                              else "none recorded for these kernel sources",
+            "k1_ms_median": k1["median_ms"],
+            "k1_ms_p10": k1["p10_ms"],
+            "k1_ms_p90": k1["p90_ms"],
+            "k1_ms_mean": k1["mean_ms"],
+            "k1_samples": k1["n"],
             "bytes_per_launch": lk["bytes"],
         },
         "e2e": e2e,
         "gpu_launches": 2 * K,                 # row statistics + selection per step
-        "clocks": clocks.summary(),
+        "clocks": m["clocks"],
     }
+    if rank == 0 and world == 1 and not args.no_extras and lk["name"] == "bf16":
+        out["workloads"] = extras(args, device, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -617,30 +673,22 @@ def measured_tensor_peak():
         return 1400.0, 1800.0, "fallback"
 
 
-def run_fused(args, rank, world, local):
-    """One step = eb_unembed_sample over B x 256 fresh all-masked positions (B = 4, or 1 for
-    the small-batch workload): h [256 B, 2048] x W [2048, 262144] on the tensor cores, the row
-    statistics in the epilogue, the selection.  h and W are resident (W is the model's
-    unembedding matrix); each graph replay restores the canvas states first."""
-    import ctypes
-
+def measure_fused(FB, K, Wm, e2e_steps, device, local, dist=None, world=1):
+    """One step = eb_unembed_sample over FB x 256 fresh all-masked positions: h [256 FB, 2048]
+    x W [2048, 262144] on the tensor cores, the row statistics in the epilogue, the selection.
+    h and W are resident (W is the model's unembedding matrix); each graph replay restores the
+    canvas states first.  Returns the measurement dict (the line's fields)."""
     import torch
 
     import canvas_sampler_step_b300 as eb
     import eb_synth.device as synth_dev
 
-    FB = 1 if args.workload == "fused1" else 4
     FUSED_FLOP = 2 * FB * FL * FK * FV
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
     lib = eb.lib()
-    synth_dev.lib()
     stream = torch.cuda.current_stream(device)
     h = torch.empty((FB * FL, FK), dtype=torch.int16, device=device)
     W = torch.empty((FK, FV), dtype=torch.int16, device=device)
     synth_dev.unembed_inputs(0, FB * FL, FK, FV, 0.02, 0.05, h, W)
-    K, Wm = args.steps, args.warmup
     N = max(d for d in range(1, min(K, 20) + 1) if K % d == 0)
     R = K // N
     canv = [eb.Canvas(FB, FL, FV, eb.EB_BF16, device=device) for _ in range(N)]
@@ -683,26 +731,28 @@ def run_fused(args, rank, world, local):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(dist, local)
+    k3_ms = []
     with ClockSampler(local) as clocks:
         start.record(stream)
         for _ in range(R):
             graph.replay()
+            k3_ms += [b.elapsed_time(e) for b, e in zip(kb, ke)] if False else []
         end.record(stream)
         torch.cuda.synchronize()
     barrier(dist, local)
     elapsed = start.elapsed_time(end) / 1e3
-    k3_ms = [b.elapsed_time(e) for b, e in zip(kb, ke)]
+    k3_ms = [b.elapsed_time(e) for b, e in zip(kb, ke)]          # the last replay's steps
     value, slowest = aggregate(K, elapsed, world, dist, local)
     for c in canv:
         if not ((c.status == 0).all() and (c.committed >= 1).all()):
             raise RuntimeError("timed steps did not run the expected workload")
     sustained, burst, kind = measured_tensor_peak()
-    k3_s = statistics.mean(k3_ms) / 1e3
-    achieved = FUSED_FLOP / k3_s / 1e12
+    k3 = sample_stats(k3_ms)
+    achieved = FUSED_FLOP / (k3["median_ms"] / 1e3) / 1e12
 
     # end to end: per step the hidden states and canvas state go host -> device, the step
     # runs, the results come back (W stays resident: it is the model's weight)
-    n_e2e = max(1, min(args.e2e_steps, 50))
+    n_e2e = max(1, min(e2e_steps, 50))
     h_host = h.cpu().pin_memory()
     in_keys = ("mask", "tokens", "prev_argmax", "status")
     hstate = {k: pristine[k].cpu().pin_memory() for k in in_keys}
@@ -729,31 +779,27 @@ def run_fused(args, rank, world, local):
     e2e_value, _ = aggregate(n_e2e, e0.elapsed_time(e1) / 1e3, world, dist, local)
     h2d = h_host.numel() * 2 + sum(v.numel() * v.element_size() for v in hstate.values())
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
-    out = {
-        "metric": FUSED_METRIC.format(B=FB), "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": slowest * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded Philox / Box-Muller h and W, eb_synth)",
+    del W, h, h_dev
+    return {
+        "metric": FUSED_METRIC.format(B=FB), "value": value, "unit": "steps/s", "steps": K,
+        "warmup": Wm, "ms_per_step": slowest * 1e3 / K, "higher_is_better": True, "dtype": "bf16",
         "config": {"workload": f"fused unembedding + EB sampler step: h [{FB * FL}, 2048] ~ N(0,1) x W "
                                "[2048, 262144] ~ N(0, 0.02^2) + 0.05 planted per row, bf16, "
                                f"{FB} canvas{'es' if FB > 1 else ''} x 256 positions all masked, T=0.8",
                    "B": FB, "L": FL, "K": FK, "V": FV,
                    "l2": "W (1 GiB) > 126 MB L2, read once per step",
-                   "launch": f"CUDA graph of {N} steps (+ canvas-state restores) replayed {R} times",
-                   "parallelism": f"replicas x{world}"},
+                   "launch": f"CUDA graph of {N} steps (+ canvas-state restores) replayed {R} times; "
+                             "the fused kernel timed by events around each step of the last replay"},
         "roofline": {"bound": "tensor", "kernel": "k3_unembed", "achieved": achieved,
                      "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
                      "peak_kind": f"{kind} bf16 sustained (burst {burst})", "traffic": None,
-                     "k3_ms_mean": statistics.mean(k3_ms), "flop_per_launch": FUSED_FLOP},
+                     "k3_ms_median": k3["median_ms"], "k3_ms_p10": k3["p10_ms"], "k3_ms_p90": k3["p90_ms"],
+                     "k3_samples": k3["n"], "flop_per_launch": FUSED_FLOP},
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": n_e2e, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
     }
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
 
 
 # ------------------------------------------------------------------ block driver workload
@@ -762,7 +808,7 @@ BLOCKS_METRIC = ("EB block driver (continuous batching): blocks/s over 64 blocks
                  "on 8 slots, stand-in denoiser included")
 
 
-def run_blocks(args, rank, world, local):
+def measure_blocks(device, local, dist=None, world=1):
     """eb_sample_blocks: 64 blocks (peak growth 0.1-0.8, so they stop after different step
     counts) on 8 slots; a freed slot takes the next block while the others keep denoising.
     The stand-in denoiser regenerates the occupied slots' logits on the device every iteration."""
@@ -774,11 +820,6 @@ def run_blocks(args, rank, world, local):
     import eb_synth
     import eb_synth.device as synth_dev
 
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
-    eb.lib()
-    synth_dev.lib()
     stream = torch.cuda.current_stream(device)
     n, slots = 64, 8
     cfg = eb_synth.cfg3(B=n)
@@ -810,14 +851,12 @@ def run_blocks(args, rank, world, local):
     elapsed = start.elapsed_time(end) / 1e3
     value, slowest = aggregate(n, elapsed, world, dist, local)
     st = steps.cpu().numpy()
-    out = {
-        "metric": BLOCKS_METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": n,
-        "warmup": 1, "ms_per_step": slowest * 1e3 / n, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded Philox / Box-Muller stand-in denoiser, eb_synth)",
+    return {
+        "metric": BLOCKS_METRIC, "value": value, "unit": "blocks/s", "steps": n,
+        "warmup": 1, "ms_per_step": slowest * 1e3 / n, "higher_is_better": True, "dtype": "f32",
         "config": {"workload": "block driver: 64 blocks x 256 positions x 262144 bf16, sigma 3, peak "
                                "U(0,4) + r s, r in (0.1, 0.2, 0.4, 0.8), up to 48 steps each, 8 slots",
-                   "slots": slots, "iterations": iters, "parallelism": f"replicas x{world}"},
+                   "slots": slots, "iterations": iters},
         "canvas_steps_per_s": float(st.sum()) / slowest,
         "slot_occupancy": float(st.sum()) / (iters * slots),
         "steps_to_stop_mean": float(st.mean()),
@@ -825,24 +864,119 @@ def run_blocks(args, rank, world, local):
         "gpu_launches": None,
         "clocks": clocks.summary(),
     }
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
 
 
-# ------------------------------------------------------------------ adaptive loop workload
+# ------------------------------------------------------------------ adaptive loop workloads
 
-LOOP_METRIC = ("EB adaptive denoising loop: canvas-steps/s over 8 canvases x 256 x 262144 bf16 "
-               "(peak growth 0.1-0.8), stand-in denoiser included")
+LOOP_METRIC = ("EB adaptive denoising loop: canvas-steps/s over {B} canvas{es} x 256 x 262144 bf16 ({what}), "
+               "stand-in denoiser included")
 
 
-def run_loop(args, rank, world, local):
-    """The whole <= 48-step loop (eb_sample_canvas) over 8 canvases whose logits the seeded
-    stand-in denoiser regenerates on the device every step; reports steps to stop per canvas
-    and positions committed per step.  One 'step' of the metric is one canvas-step."""
+def measure_loop(cfg, label, runs, warm, device, local, dist=None, world=1):
+    """The whole <= 48-step loop (eb_sample_canvas) over cfg.B canvases whose logits the seeded
+    stand-in denoiser regenerates on the device every step; reports steps to stop per canvas and
+    positions committed per step.  One 'step' of the metric is one canvas-step."""
     import ctypes
 
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth.device as synth_dev
+
+    stream = torch.cuda.current_stream(device)
+    recipe = synth_dev.Recipe.of(cfg)
+    buf = torch.empty((cfg.B, cfg.L, cfg.V), dtype=torch.int16, device=device)
+    params = eb.eb_default_params(seed=int(cfg.seeds[0]))
+
+    def loop(c):
+        return c.run(params, synth_dev.callback_address(), ctypes.addressof(recipe), buf, poll_every=4)
+
+    for _ in range(warm):
+        loop(eb.Canvas(cfg.B, cfg.L, cfg.V, eb.EB_BF16, device=device))
+    # fresh canvases made before the timed region; every loop is timed by its own events
+    canv = [eb.Canvas(cfg.B, cfg.L, cfg.V, eb.EB_BF16, device=device) for _ in range(runs)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    with ClockSampler(local) as clocks:
+        for c, (b, e) in zip(canv, ev):
+            b.record(stream)
+            loop(c)
+            e.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist, local)
+    loop_ms = [b.elapsed_time(e) for b, e in ev]
+    canvas_steps = sum(int(c.steps_taken.sum().item()) for c in canv)
+    elapsed = sum(loop_ms) / 1e3
+    c = canv[-1]
+    value, slowest = aggregate(canvas_steps, elapsed, world, dist, local)
+    st = c.steps_taken.cpu().numpy().tolist()
+    com = c.committed_per_step.cpu().numpy()
+    per_step = [[int(v) for v in row[:n]] for row, n in zip(com, st)]
+    return {
+        "metric": LOOP_METRIC.format(B=cfg.B, es="es" if cfg.B > 1 else "", what=label), "value": value,
+        "unit": "canvas-steps/s", "steps": canvas_steps, "warmup": warm,
+        "ms_per_step": slowest * 1e3 / canvas_steps, "higher_is_better": True, "dtype": "f32",
+        "config": {"workload": f"adaptive loop ({label}): {cfg.B} canvas{'es' if cfg.B > 1 else ''} x 256 "
+                               f"positions x 262144 bf16, sigma {cfg.sigma:g}, peak U({cfg.base_lo:g},"
+                               f"{cfg.base_lo + cfg.base_scale:g}) + r s, r in {sorted(set(cfg.growth))}, "
+                               "up to 48 steps, logits regenerated on the device every step",
+                   "loops": runs},
+        "loop_ms_median": float(np.median(loop_ms)),
+        "steps_to_stop": st,
+        "stop_reason": c.status.cpu().numpy().tolist(),
+        "committed_per_step": per_step if cfg.B == 1 else None,
+        "tokens_committed_per_step_mean": float(com[com > 0].mean()) if (com > 0).any() else 0.0,
+        "tokens_committed_per_step_by_canvas": [float(cfg.L) / n for n in st],
+        "gpu_launches": None,
+        "clocks": clocks.summary(),
+    }
+
+
+# ------------------------------------------------------------------ all workloads in one run
+
+def extras(args, device, local):
+    """The per-workload records of the headline line, each measured here on the same GPU."""
+    import dataclasses
+
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import eb_synth
+    out = {}
+    out["fused"] = measure_fused(4, 20, 3, 10, device, local)
+    torch.cuda.empty_cache()
+    out["fused1"] = measure_fused(1, 40, 3, 10, device, local)
+    torch.cuda.empty_cache()
+    out["loop_b1"] = measure_loop(eb_synth.cfg2(), "full adaptive loop, one canvas, peak growth 0.3", 5, 1,
+                                  device, local)
+    out["loop_b8"] = measure_loop(eb_synth.cfg3(), "mixed batch of eight, peak growth 0.1-0.8", 3, 1,
+                                  device, local)
+    torch.cuda.empty_cache()
+    fp8 = argparse.Namespace(**{**vars(args), "logits": "fp8", "steps": 200, "warmup": 5})
+    lk = logits_kind(fp8, eb, torch)
+    m = run_single(fp8, lk, device, local, None, 1)
+    peak, _ = measured_peaks()
+    out["e4m3"] = {
+        "metric": lk["metric"], "value": m["value"], "unit": "steps/s", "steps": m["K"],
+        "ms_per_step": m["slowest"] * 1e3 / m["K"], "higher_is_better": True, "dtype": "f32",
+        "config": {"workload": lk["workload"], "logits_dtype": "e4m3"},
+        "roofline": {"bound": "hbm", "kernel": "k1_rowstats<e4m3>",
+                     "achieved": lk["bytes"] / (m["k1"]["median_ms"] / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": lk["bytes"] / (m["k1"]["median_ms"] / 1e3) / 1e9 / peak,
+                     "k1_ms_median": m["k1"]["median_ms"], "k1_ms_p10": m["k1"]["p10_ms"],
+                     "k1_ms_p90": m["k1"]["p90_ms"], "k1_samples": m["k1"]["n"],
+                     "bytes_per_launch": lk["bytes"]},
+        "clocks": m["clocks"],
+    }
+    del m
+    torch.cuda.empty_cache()
+    out["blocks"] = measure_blocks(device, local)
+    return out
+
+
+def run_workload(args, rank, world, local):
+    """`--workload NAME`: one of the other workloads as the printed line."""
     import torch
 
     import canvas_sampler_step_b300 as eb
@@ -854,54 +988,24 @@ def run_loop(args, rank, world, local):
     dist = init_dist(world, "nccl")
     eb.lib()
     synth_dev.lib()
-    stream = torch.cuda.current_stream(device)
-    cfg = eb_synth.cfg3()
-    recipe = synth_dev.Recipe.of(cfg)
-    buf = torch.empty((cfg.B, cfg.L, cfg.V), dtype=torch.int16, device=device)
-    params = eb.eb_default_params(seed=0)
-    runs = max(1, args.steps // 200)
-
-    def loop():
-        c = eb.Canvas(cfg.B, cfg.L, cfg.V, eb.EB_BF16, device=device)
-        ran = c.run(params, synth_dev.callback_address(), ctypes.addressof(recipe), buf, poll_every=4)
-        return c, ran
-
-    for _ in range(max(1, args.warmup // 100)):
-        loop()
-    torch.cuda.synchronize()
-    barrier(dist, local)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    canvas_steps = 0
-    with ClockSampler(local) as clocks:
-        start.record(stream)
-        for _ in range(runs):
-            c, ran = loop()
-            canvas_steps += int(c.steps_taken.sum().item())
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier(dist, local)
-    elapsed = start.elapsed_time(end) / 1e3
-    value, slowest = aggregate(canvas_steps, elapsed, world, dist, local)
-    st = c.steps_taken.cpu().numpy().tolist()
-    com = c.committed_per_step.cpu().numpy()
-    out = {
-        "metric": LOOP_METRIC, "value": value, "unit": "canvas-steps/s", "n_gpus": world,
-        "steps": canvas_steps, "warmup": args.warmup, "ms_per_step": slowest * 1e3 / canvas_steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded Philox / Box-Muller stand-in denoiser, eb_synth)",
-        "config": {"workload": "adaptive loop: 8 canvases x 256 positions x 262144 bf16, sigma 3, "
-                               "peak U(0,4) + r s, r in (0.1, 0.2, 0.4, 0.8), up to 48 steps, "
-                               "logits regenerated on the device every step",
-                   "loops": runs, "parallelism": f"replicas x{world}"},
-        "steps_to_stop": st,
-        "stop_reason": c.status.cpu().numpy().tolist(),
-        "committed_per_step_mean": float(com[com > 0].mean()) if (com > 0).any() else 0.0,
-        "gpu_launches": None,
-        "clocks": clocks.summary(),
-    }
+    if args.workload in ("fused", "fused1"):
+        FB = 1 if args.workload == "fused1" else 4
+        out = measure_fused(FB, args.steps, args.warmup, args.e2e_steps, device, local, dist, world)
+    elif args.workload in ("loop", "loop1"):
+        cfg = eb_synth.cfg3() if args.workload == "loop" else eb_synth.cfg2()
+        label = ("mixed batch of eight, peak growth 0.1-0.8" if args.workload == "loop"
+                 else "full adaptive loop, one canvas, peak growth 0.3")
+        out = measure_loop(cfg, label, max(1, args.steps // 200), max(1, args.warmup // 100), device, local,
+                           dist, world)
+    else:
+        out = measure_blocks(device, local, dist, world)
+    line = {"metric": out.pop("metric"), "value": out.pop("value"), "unit": out.pop("unit"), "n_gpus": world}
+    line.update(out)
+    line.update({"scaling": "weak", "vs_baseline": None,
+                 "data": "synthetic (seeded Philox / Box-Muller inputs, eb_synth)"})
+    line["config"]["parallelism"] = f"replicas x{world}"
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -911,14 +1015,10 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
-    elif args.workload in ("fused", "fused1"):
-        run_fused(args, rank, world, local)
-    elif args.workload == "loop":
-        run_loop(args, rank, world, local)
-    elif args.workload == "blocks":
-        run_blocks(args, rank, world, local)
-    else:
+    elif args.workload == "single":
         run_ours(args, rank, world, local)
+    else:
+        run_workload(args, rank, world, local)
 
 
 if __name__ == "__main__":

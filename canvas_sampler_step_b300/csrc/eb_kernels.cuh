@@ -53,7 +53,7 @@ constexpr int kK2Threads = 256;
 constexpr int kMaxL = 1024;
 constexpr int kMaxGrid = 8192;
 constexpr int kWeightUnmasked = 11;                // relative cost of a vector of an unmasked row
-constexpr int kWeightMasked = 26;                  // ... and of a masked row (measured 2.36 : 1)
+constexpr int kWeightMasked = 33;                  // ... and of a masked row (3 : 1, tuned on the mixed step)
 constexpr uint32_t kWaitLimit = 1u << 26;           // mbarrier polls before giving up
 constexpr uint32_t kDiagWaitLimit = 1u << 12;       // ... under the diagnostic stall flag
 
@@ -242,11 +242,108 @@ __device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, u
     return make_uint4(c0, c1, c2, c3);
 }
 
+// Row constants of Philox4x32-10 along one canvas row.  Counter words 1-3 (position p, step
+// s, stream and canvas sw) are the same for every block of a row, so round 0's product of word
+// 2, round 0's new word 0 and round 1's product of that word depend on the row alone; the
+// xor partners below fold them with the round keys.
+struct PhiloxRow {
+    uint32_t c1x;   // round 0: sw ^ k0'   (partner of hi(M0 c0))
+    uint32_t c2x;   // round 1: lo(M1 s) ^ k1  (partner of hi(M1 c2))
+    uint32_t c3x;   // round 1: hi(M0 n0) ^ k1' (partner of c3)
+    uint32_t c5x;   // round 2: lo(M0 n0) ^ k2' (partner of hi(M0 c0))
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t p, uint32_t s, uint32_t sw, const RoundKeys &K)
+{
+    const uint64_t ps = (uint64_t)0xCD9E8D57u * s;
+    const uint32_t n0 = (uint32_t)(ps >> 32) ^ p ^ K.k[0];      // round 0's new word 0
+    const uint64_t pn = (uint64_t)0xD2511F53u * n0;               // round 1's first product
+    PhiloxRow r;
+    r.c1x = sw ^ K.k[1];
+    r.c2x = (uint32_t)ps ^ K.k[2];
+    r.c3x = (uint32_t)(pn >> 32) ^ K.k[3];
+    r.c5x = (uint32_t)pn ^ K.k[5];
+    return r;
+}
+
+// Philox4x32-10 of counter (c0, p, s, sw) from the row constants of (p, s, sw): the same
+// words as philox(c0, p, s, sw, K), with the row-constant work of rounds 0-2 left out.
+__device__ __forceinline__ uint4 philox_row_block(uint32_t c0, const PhiloxRow &R, const RoundKeys &K)
+{
+    const uint64_t a = (uint64_t)0xD2511F53u * c0;                // round 0
+    const uint32_t x2 = (uint32_t)(a >> 32) ^ R.c1x;
+    const uint32_t x3 = (uint32_t)a;
+    const uint64_t b = (uint64_t)0xCD9E8D57u * x2;                // round 1
+    uint32_t w0 = (uint32_t)(b >> 32) ^ R.c2x;
+    uint32_t w1 = (uint32_t)b;
+    uint32_t w2 = x3 ^ R.c3x;
+    uint32_t w3;
+    {                                                              // round 2
+        const uint64_t p0 = (uint64_t)0xD2511F53u * w0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * w2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ w1 ^ K.k[4];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ R.c5x;
+        w1 = (uint32_t)p1;
+        w3 = (uint32_t)p0;
+        w0 = n0;
+        w2 = n2;
+    }
+#pragma unroll
+    for (int r = 3; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * w0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * w2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ w1 ^ K.k[2 * r];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ w3 ^ K.k[2 * r + 1];
+        w1 = (uint32_t)p1;
+        w3 = (uint32_t)p0;
+        w0 = n0;
+        w2 = n2;
+    }
+    return make_uint4(w0, w1, w2, w3);
+}
+
 // f = 1 + (0x7FFFFF - j) 2^-23 for j = low 23 bits of w, so that 1 - u = f - (1 - 2^-24)
 // exactly, u = (j + 1/2) 2^-23 being the entry's uniform.
 __device__ __forceinline__ float one_minus_u_plus(uint32_t w)
 {
     return __uint_as_float((w & 0x7FFFFFu) ^ 0x3FFFFFFFu);
+}
+
+// u' = 1 + j 2^-23 for j = low 23 bits of w: then 1 - u = 2 - u' - 2^-24 exactly.  An entry can
+// beat the best score only if 1 - u < e K (e = 2^t, K = cand_scale), i.e. u' + e K > 2 - 2^-24; a
+// single rounding of u' + e K then gives a value >= 2, which sets bit 30 of its binary32 bits.
+__device__ __forceinline__ float u_prime(uint32_t w)
+{
+    return __uint_as_float((w & 0x7FFFFFu) | 0x3F800000u);
+}
+
+constexpr uint32_t kCandBit = 0x40000000u;          // set in bits(u' + e K) iff it is >= 2 (or NaN)
+
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The exact Gumbel score z - ln(-ln u) of one entry (x its logit, w its Philox word).
+__device__ __forceinline__ float gumbel_score(float x, uint32_t w, float invT)
+{
+    const float delta = (2.0f - u_prime(w)) - 5.9604644775390625e-8f;   // 1 - u, exact
+    const float E = -log1pf(-delta);                                     // -ln u
+    return x * invT - logf(E);
+}
+
+// A cheap estimate of the same score, within 2e-5 of it: ln E from lg2.approx, and -ln u from
+// its series for 1 - u < 2^-5 (relative error < 8e-6), else from lg2.approx of u.
+__device__ __forceinline__ float gumbel_score_estimate(float x, uint32_t w, float invT)
+{
+    const float up = u_prime(w);
+    const float delta = (2.0f - up) - 5.9604644775390625e-8f;
+    float E;
+    if (delta < 0.03125f) E = delta * fmaf(delta, fmaf(delta, 0.333333343f, 0.5f), 1.0f);
+    else E = -lg2_approx(1.0f - delta) * kLn2;
+    return fmaf(-lg2_approx(E), kLn2, x * invT);
 }
 
 __device__ __forceinline__ float cand_scale(float xm, float best, float c)
@@ -300,17 +397,28 @@ __device__ __forceinline__ void warp_merge(RowState &st, float c)
     }
 }
 
+// Order-preserving unsigned key of a binary32 value (larger key = larger value; -0 and +0
+// share +0's key; NaN takes key 0, below -inf, so that a maximum never picks it).
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return f != f ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+}
+
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// The warp's best (score, index) by the order of better(): the largest score, then the lowest
+// index (as unsigned, so -1 = none comes last), in two warp-wide reductions.
 __device__ __forceinline__ void warp_best(float &best, int &bi)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (better(ob, oi, best, bi)) {
-            best = ob;
-            bi = oi;
-        }
-    }
+    const uint32_t k = order_key(best);
+    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, k);
+    const uint32_t imin = __reduce_min_sync(0xFFFFFFFFu, k == kmax ? (uint32_t)bi : 0xFFFFFFFFu);
+    best = key_value(kmax);
+    bi = (int)imin;
 }
 
 __device__ __forceinline__ RowState empty_state()
@@ -440,6 +548,43 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
             const float score = x[j] * invT - logf(E);
             const int idx = (int)(v0 + (uint32_t)j);
             if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
+        }
+    }
+    return best;
+}
+
+// The best exact score over the warp's lanes of one entry each (x, w, index idx): the seed of a
+// segment's best score.  Out of line: it runs once per segment.
+__device__ __noinline__ GumbelBest gumbel_seed(float x, uint32_t w, float invT, int idx)
+{
+    float sb = gumbel_score(x, w, invT);
+    if (sb != sb) sb = -INFINITY;
+    warp_best(sb, idx);
+    return GumbelBest{sb, sb == -INFINITY ? -1 : idx};
+}
+
+// The streaming kernel's exact pass over a group of N logits (entries v0 ..) of a lane whose
+// candidate test passed: every entry with bits(u' + e K) & kCandBit takes a score estimate, and
+// only an entry whose estimate comes within a margin of the best score takes the exact score
+// (the margin, 1e-4 + |best| 2^-20, exceeds the estimate's error and the rounding of either
+// score).  2^t is recomputed from the logits exactly as the batch computed it.
+template <int N>
+__device__ __noinline__ GumbelBest gumbel_exact_filtered(float4 xa, float4 xb, uint4 wa, uint4 wb, uint32_t v0,
+                                                         float c, float invT, float nb, float K, GumbelBest best)
+{
+    const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float e = ex2(fmaf(x[j], c, nb));
+        if (__float_as_uint(fmaf(e, K, u_prime(w[j]))) & kCandBit) {
+            const float est = gumbel_score_estimate(x[j], w[j], invT);
+            const float margin = fmaf(fabsf(best.score), 9.5367431640625e-7f, 1.0e-4f);
+            if (!(est < best.score - margin)) {
+                const float score = gumbel_score(x[j], w[j], invT);
+                const int idx = (int)(v0 + (uint32_t)j);
+                if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
+            }
         }
     }
     return best;
@@ -615,7 +760,7 @@ __device__ __forceinline__ void consume_packed(const uint4 r, bool valid, uint32
     }
 }
 
-// Largest of N floats (N = 4, 8 or 16) with three-input maxima.
+// Largest of N floats (N = 4, 8, 16 or 32) with three-input maxima.
 template <int N>
 __device__ __forceinline__ float vec_max(const float (&x)[N])
 {
@@ -623,11 +768,17 @@ __device__ __forceinline__ float vec_max(const float (&x)[N])
         return max3(x[0], x[1], fmaxf(x[2], x[3]));
     } else if constexpr (N == 8) {
         return max3(max3(x[0], x[1], x[2]), max3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
-    } else {
-        static_assert(N == 16, "vec_max: N is 4, 8 or 16");
+    } else if constexpr (N == 16) {
         const float m0 = max3(x[0], x[1], x[2]), m1 = max3(x[3], x[4], x[5]), m2 = max3(x[6], x[7], x[8]);
         const float m3 = max3(x[9], x[10], x[11]), m4 = max3(x[12], x[13], x[14]);
         return max3(max3(m0, m1, m2), m3, fmaxf(m4, x[15]));
+    } else {
+        static_assert(N == 32, "vec_max: N is 4, 8, 16 or 32");
+        float m[11];
+#pragma unroll
+        for (int i = 0; i < 10; ++i) m[i] = max3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+        m[10] = fmaxf(x[30], x[31]);
+        return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), max3(max3(m[6], m[7], m[8]), m[9], m[10]));
     }
 }
 
@@ -635,12 +786,12 @@ __device__ __forceinline__ float vec_max(const float (&x)[N])
 // from (jv0 + 32 u) VEC on.  The arithmetic per entry is that of consume_vals (the warp shares
 // one running maximum and one best Gumbel score), but a whole batch takes one new-maximum vote
 // and, for a masked row, one candidate vote.  The Philox blocks of all U vectors are drawn
-// first, in the same basic block as the unpacking and the maximum, so that their independent
-// chains overlap with the rest.
+// after the new-maximum vote, in the same basic block as the exponentials and the sums, so
+// that their independent chains overlap with the rest.
 template <int VEC, int U, bool MASKED>
 __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0, const K1Args &a, const RowCtx &rc,
-                                              f32x2 c2, RowState &st, PackedSums &q, float &nb,
-                                              f32x2 &nb2, float &K)
+                                              const PhiloxRow &ph, f32x2 c2, RowState &st, PackedSums &q,
+                                              float &nb, f32x2 &nb2, float &K)
 {
     constexpr int N = U * VEC;
     float x[N];
@@ -665,42 +816,51 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
             x[4 * u + 3] = __uint_as_float(r[u].w);
         }
     }
-    uint32_t w[MASKED ? N : 1];
-    if constexpr (MASKED) {
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int k = 0; k < VEC / 4; ++k) {
-                const uint4 g = philox((jv0 + 32u * (uint32_t)u) * (uint32_t)(VEC / 4) + (uint32_t)k, rc.p,
-                                       rc.step, rc.sw, a.keys);
-                w[VEC * u + 4 * k + 0] = g.x;
-                w[VEC * u + 4 * k + 1] = g.y;
-                w[VEC * u + 4 * k + 2] = g.z;
-                w[VEC * u + 4 * k + 3] = g.w;
-            }
-    }
     const float vmax = vec_max<N>(x);
     if (__any_sync(0xFFFFFFFFu, vmax > st.xm)) {
-        float wm = vmax;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+        const float wm = key_value(__reduce_max_sync(0xFFFFFFFFu, order_key(vmax)));
         // first entry holding it: this lane's entries grow with the vector, then the entry, and
         // all of the warp's vector u precede its vector u + 1
-        int idx = 0x7FFFFFFF;
+        uint32_t idx = 0x7FFFFFFFu;
         if (vmax == wm) {
 #pragma unroll
             for (int i = N - 1; i >= 0; --i)
-                if (x[i] == wm) idx = (int)((jv0 + 32u * (uint32_t)(i / VEC)) * (uint32_t)VEC + (uint32_t)(i % VEC));
+                if (x[i] == wm) idx = (jv0 + 32u * (uint32_t)(i / VEC)) * (uint32_t)VEC + (uint32_t)(i % VEC);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
+        idx = __reduce_min_sync(0xFFFFFFFFu, idx);
         const float d = (st.xm - wm) * rc.c;
         packed_rescale(q, d, ex2(d));
         st.ai = idx;
         st.xm = wm;
         nb = -wm * rc.c;
         nb2 = pk2(nb, nb);
-        if (MASKED) K = cand_scale(st.xm, st.best, rc.c);
+        if constexpr (MASKED) {
+            if (st.best == -INFINITY) {
+                // the segment's first batch: every lane's first entry seeds the best score, so
+                // that the candidate test has a finite score to beat from the start
+                const uint32_t w0 = philox_row_block(jv0 * (uint32_t)(VEC / 4), ph, a.keys).x;
+                const GumbelBest g = gumbel_seed(x[0], w0, rc.invT, (int)(jv0 * (uint32_t)VEC));
+                st.best = g.score;
+                st.bi = g.idx;
+            }
+            K = cand_scale(st.xm, st.best, rc.c);
+        }
+    }
+    // the Philox words of the batch's entries (masked rows), drawn after the vote so that they
+    // are not live across its branch; their chains interleave with the exponentials below
+    uint32_t w[MASKED ? N : 1];
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < VEC / 4; ++k) {
+                const uint4 g = philox_row_block((jv0 + 32u * (uint32_t)u) * (uint32_t)(VEC / 4) + (uint32_t)k, ph,
+                                                 a.keys);
+                w[VEC * u + 4 * k + 0] = g.x;
+                w[VEC * u + 4 * k + 1] = g.y;
+                w[VEC * u + 4 * k + 2] = g.z;
+                w[VEC * u + 4 * k + 3] = g.w;
+            }
     }
     float e[N];
 #pragma unroll
@@ -720,20 +880,26 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
         }
     }
     if constexpr (MASKED) {
-        bool cand[U];
-        bool any = false;
-        // the threshold 2^t K + (1 + 2^-23) of two entries at a time
-        const f32x2 K2 = pk2(K, K), A2 = pk2(kCandAdd, kCandAdd);
+        // candidate test of two entries at a time: u' + 2^t K on packed FMA, the results' bits
+        // or-ed together; bit 30 of the or is set iff some entry's sum reached 2
+        uint32_t cacc[U];
+        const f32x2 K2 = pk2(K, K);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            cand[u] = false;
+            cacc[u] = 0u;
 #pragma unroll
             for (int j = 0; j < VEC; j += 2) {
-                float h0, h1;
-                upk2(fma2(pk2(e[VEC * u + j], e[VEC * u + j + 1]), K2, A2), h0, h1);
-                cand[u] |= one_minus_u_plus(w[VEC * u + j]) < h0;
-                cand[u] |= one_minus_u_plus(w[VEC * u + j + 1]) < h1;
+                float d0, d1;
+                upk2(fma2(pk2(e[VEC * u + j], e[VEC * u + j + 1]), K2,
+                          pk2(u_prime(w[VEC * u + j]), u_prime(w[VEC * u + j + 1]))), d0, d1);
+                cacc[u] |= __float_as_uint(d0) | __float_as_uint(d1);
             }
+        }
+        bool cand[U];
+        bool any = false;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            cand[u] = (cacc[u] & kCandBit) != 0u;
             any |= cand[u];
         }
         if (__any_sync(0xFFFFFFFFu, any)) {
@@ -753,7 +919,7 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
                         const uint4 wb = G8 == 8 ? make_uint4(w[o + (G8 > 4 ? 4 : 0)], w[o + (G8 > 5 ? 5 : 0)],
                                                               w[o + (G8 > 6 ? 6 : 0)], w[o + (G8 > 7 ? 7 : 0)])
                                                  : make_uint4(0u, 0u, 0u, 0u);
-                        const GumbelBest g = gumbel_exact_group<G8>(
+                        const GumbelBest g = gumbel_exact_filtered<G8>(
                             xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC + (uint32_t)(G8 * h), rc.c, rc.invT,
                             nb, K, GumbelBest{st.best, st.bi});
                         st.best = g.score;

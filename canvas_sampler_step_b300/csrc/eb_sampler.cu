@@ -11,6 +11,8 @@
 #include <cstring>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "eb_kernels.cuh"
 #include "eb_sampler.h"
 
@@ -285,11 +287,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 // The nfull whole batches of a segment starting at vector j0.  The thread's staging slot for
 // ring position d and vector u is at sbase + d kDepthStride + u kSlotStride; the ring offset
 // and the global pointer advance by constants, so that no slot or address is recomputed from
-// the batch index.
+// the batch index.  One copy of the batch body, so that the masked and unmasked loops of the
+// SM's warps stay in the instruction cache together.
 template <int VEC, int U, bool MASKED>
 __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t nfull,
-                                              const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
-                                              float &nb, f32x2 &nb2, float &K, uint32_t sbase)
+                                              const RowCtx &rc, const PhiloxRow &ph, f32x2 c2, RowState &st,
+                                              PackedSums &q, float &nb, f32x2 &nb2, float &K, uint32_t sbase)
 {
     constexpr uint32_t kBatch = 32u * U;
     constexpr uint32_t kSlotStride = kDirectThreads * 16u;
@@ -313,6 +316,7 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
     uint32_t jv = j0 + lane;
     // batches b < nfull - (depth - 1) still prefetch batch b + depth - 1
     const uint32_t npre = nfull > (uint32_t)(kAsyncDepth - 1) ? nfull - (uint32_t)(kAsyncDepth - 1) : 0u;
+#pragma unroll 1
     for (uint32_t b = 0; b < nfull; ++b) {
         if (b < npre) {
             const uint32_t offn = (off + (uint32_t)(kAsyncDepth - 1) * kDepthStride) & (kRing - 1);
@@ -325,7 +329,7 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r[u] = lds128(sbase + off + (uint32_t)u * kSlotStride);
-        consume_batch<VEC, U, MASKED>(r, jv, a, rc, c2, st, q, nb, nb2, K);
+        consume_batch<VEC, U, MASKED>(r, jv, a, rc, ph, c2, st, q, nb, nb2, K);
         off = (off + kDepthStride) & (kRing - 1);
         jv += kBatch;
     }
@@ -351,8 +355,12 @@ __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src,
     const uint32_t jf = j0 + nfull * kBatch;
     const uint32_t sbase = smem_addr(stage) + threadIdx.x * 16u;
     if (nfull > 0) {
-        if (gumbel) async_batches<VEC, U, true>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
-        else async_batches<VEC, U, false>(a, src, j0, nfull, rc, c2, st, q, nb, nb2, K, sbase);
+        if (gumbel) {
+            const PhiloxRow ph = philox_row(rc.p, rc.step, rc.sw, a.keys);
+            async_batches<VEC, U, true>(a, src, j0, nfull, rc, ph, c2, st, q, nb, nb2, K, sbase);
+        } else {
+            async_batches<VEC, U, false>(a, src, j0, nfull, rc, PhiloxRow{}, c2, st, q, nb, nb2, K, sbase);
+        }
     }
     if constexpr (VEC == 16) {
         // e4m3: the tail in half vectors of 8 logits, consecutive half vectors on consecutive
@@ -565,7 +573,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     __shared__ unsigned long long red_sum[kK2Threads / 32];
     __shared__ unsigned long long red_min[kK2Threads / 32];
     __shared__ unsigned long long small_total;
-    __shared__ int n_masked, n_small, n_committed, bad_flags, all_small;
+    __shared__ int n_masked, n_small, n_gather, n_committed, bad_flags, all_small;
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -577,6 +585,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     if (tid == 0) {
         n_masked = 0;
         n_small = 0;
+        n_gather = 0;
         n_committed = 0;
         bad_flags = 0;
         all_small = 1;
@@ -688,12 +697,11 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         // adaptive stop: every still-masked position takes its argmax
         for (int p = tid; p < L; p += blockDim.x) Acc[p] = Ms[p];
     } else if (nm > 0) {
-        // 2. gather the low-entropy candidates
-        if (tid == 0) n_small = 0;
-        __syncthreads();
+        // 2. gather the low-entropy candidates (their own counter: n_small, which every
+        // thread read above, must not change under a lagging warp)
         for (int p = tid; p < L; p += blockDim.x) {
             if (Ms[p] && (long long)Hq[p] <= a.bound_q) {
-                const int i = atomicAdd(&n_small, 1);
+                const int i = atomicAdd(&n_gather, 1);
                 keys[i] = entropy_key(Hf[p], p);
             }
         }
@@ -834,6 +842,16 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
 namespace {
 
 thread_local std::string g_last_error;
+
+// A named NVTX range for the lifetime of the object: every C-ABI entry point and every step of
+// the loops opens one, so that a profiler's timeline shows the library's calls and steps.
+// Without an attached tool the NVTX calls return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 // One-shot CUDA events recorded around the next row-statistics launch on this thread.
 thread_local cudaEvent_t g_profile_begin = nullptr, g_profile_end = nullptr;
 
@@ -1368,6 +1386,7 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
                           uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
                           void *d_workspace, size_t workspace_bytes, void *stream)
 {
+    NvtxRange range("eb_sampler_step");
     StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
                    d_sampled, d_selected, d_committed, d_mean_entropy, nullptr, nullptr};
     eb_status st = check_common(params, B, L, V, dtype, d_logits, sb, d_workspace, workspace_bytes,
@@ -1403,11 +1422,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 namespace {
 
-struct NoallocScratch {
-    std::atomic<int> ready{0};
-    void *ptr = nullptr;
-};
-NoallocScratch g_noalloc[64];
+// The array's device address per device ordinal, null until the first call on that device.
+// Two threads that make the first call at once both look it up and store the same value.
+std::atomic<void *> g_noalloc[64];
 
 // Device address of the array on the current device (set up on the first call per device).
 eb_status noalloc_scratch(void **out)
@@ -1415,16 +1432,14 @@ eb_status noalloc_scratch(void **out)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(EB_ERR_CUDA, "cudaGetDevice failed");
     if (dev < 0 || dev >= 64) return fail(EB_ERR_UNSUPPORTED, "device index %d >= 64", dev);
-    NoallocScratch &g = g_noalloc[dev];
-    if (g.ready.load(std::memory_order_acquire) == 0) {
-        void *p = nullptr;
+    void *p = g_noalloc[dev].load(std::memory_order_acquire);
+    if (!p) {
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return fail(EB_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch: %s", cudaGetErrorString(e));
-        g.ptr = p;
-        g.ready.store(1, std::memory_order_release);
+        g_noalloc[dev].store(p, std::memory_order_release);
     }
-    *out = g.ptr;
+    *out = p;
     return EB_OK;
 }
 
@@ -1440,6 +1455,7 @@ eb_status eb_sampler_step_noalloc(const eb_params *params, int B, int L, int V, 
                                   uint8_t *d_selected, int32_t *d_committed, float *d_mean_entropy,
                                   void *stream)
 {
+    NvtxRange range("eb_sampler_step_noalloc");
     if (B > 0 && L > 0 && (long long)B * L > kNoallocRows)
         return fail(EB_ERR_UNSUPPORTED, "B*L = %lld exceeds the fixed scratch of %lld positions; use "
                     "eb_sampler_step with a caller-allocated workspace", (long long)B * L, kNoallocRows);
@@ -1464,6 +1480,7 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
                            uint8_t *d_selected, void *d_workspace, size_t workspace_bytes,
                            int poll_every, int *steps_run, void *stream)
 {
+    NvtxRange range("eb_sample_canvas");
     if (steps_run) *steps_run = 0;
     StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
                    d_sampled, d_selected, nullptr, nullptr, d_committed_per_step,
@@ -1478,6 +1495,7 @@ eb_status eb_sample_canvas(const eb_params *params, int B, int L, int V, eb_dtyp
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int ran = 0;
     for (int step = start_step; step < params->max_steps; ++step) {
+        NvtxRange step_range("eb_sample_canvas step");
         if (logits_fn(user, step, d_tokens, d_status, d_logits, stream) != 0) {
             if (steps_run) *steps_run = ran;
             return fail(EB_ERR_CALLBACK, "logits callback failed at step %d", step);
@@ -1651,6 +1669,7 @@ eb_status eb_sample_blocks(const eb_params *params, int B, int L, int V, eb_dtyp
                            void *d_workspace, size_t workspace_bytes, int poll_every, int *iterations_run,
                            void *stream)
 {
+    NvtxRange range("eb_sample_blocks");
     if (iterations_run) *iterations_run = 0;
     if (!params) return fail(EB_ERR_INVALID, "params is NULL");
     if (B < 1) return fail(EB_ERR_INVALID, "B must be >= 1 slot");
@@ -1697,6 +1716,7 @@ eb_status eb_sample_blocks(const eb_params *params, int B, int L, int V, eb_dtyp
     const long long max_iter = (long long)n_blocks * params->max_steps;
     int ran = 0;
     for (long long it = 0; it < max_iter; ++it) {
+        NvtxRange iter_range("eb_sample_blocks iteration");
         if (poll_every > 0 && it > 0 && it % poll_every == 0) {
             int32_t done = 0;
             e = cudaMemcpyAsync(&done, sl.counters + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -1764,6 +1784,7 @@ eb_status eb_unembed_sample(const eb_params *params, int B, int L, int K, int V,
                             float *d_mean_entropy, void *d_workspace, size_t workspace_bytes,
                             void *stream)
 {
+    NvtxRange range("eb_unembed_sample");
     StepBuffers sb{d_mask, d_tokens, d_prev_argmax, d_status, d_steps_taken, d_entropy, d_argmax,
                    d_sampled, d_selected, d_committed, d_mean_entropy, nullptr, nullptr};
     eb_status st = check_common(params, B, L, V, EB_BF16, d_h, sb, d_workspace, workspace_bytes,
@@ -1785,6 +1806,7 @@ eb_status eb_unembed_sample(const eb_params *params, int B, int L, int K, int V,
 eb_status eb_unembed_logits(int M, int K, int V, const void *d_h, const void *d_W, float *d_logits,
                             void *stream)
 {
+    NvtxRange range("eb_unembed_logits");
     eb_status st = check_unembed(M, K, V, d_h, d_W);
     if (st != EB_OK) return st;
     if (M == 0) return ok();

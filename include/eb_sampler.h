@@ -170,7 +170,9 @@ eb_status eb_sampler_step(const eb_params *params, int B, int L, int V, eb_dtype
  * nothing.  The call allocates no memory, neither itself nor through a library.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current, and caches it.  Make that first call before any stream capture.
+ * that device current, and caches it for the life of the process.  Make that first call before
+ * any stream capture.  A cudaDeviceReset (or any other teardown of the device's primary
+ * context) voids the cached address; this entry point is not supported after one.
  *
  * All calls share the one array, and it keeps whatever the last call left in it.  Nothing in
  * it needs to start at zero: each call overwrites what it reads later.  Two calls whose work

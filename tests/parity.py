@@ -12,6 +12,7 @@ Tolerances (the sampler step's contract):
 """
 from __future__ import annotations
 
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -42,6 +43,12 @@ def host_state(c: eb.Canvas) -> dict:
              "sampled", "selected", "committed", "mean_entropy")}
 
 
+# Every Report made while a test runs is kept here with that test's id; conftest.py prints one
+# line per report at the end of the session (and writes them to $EB_TIE_REPORT if set), so
+# that the tie counts of every parity case are reported.
+REPORTS: list = []
+
+
 @dataclass
 class Report:
     rows: int = 0
@@ -50,6 +57,15 @@ class Report:
     canvas_ties: int = 0
     tied_canvases: set = field(default_factory=set)
     max_h_err: float = 0.0
+    label: str = ""
+
+    def __post_init__(self):
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        REPORTS.append((test, self))
+
+    def line(self) -> str:
+        return (f"rows {self.rows}, row ties {self.row_ties}; canvases {self.canvases}, canvas ties "
+                f"{self.canvas_ties}; max |dH| {self.max_h_err:.3g}")
 
 
 def compare_step(g: dict, res: oracle.StepResult, ost: oracle.State, running_before: np.ndarray,

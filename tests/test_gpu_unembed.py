@@ -76,7 +76,7 @@ def _fused_vs_oracle(B, L, K, V, mask, seed=0, temperature=0.8):
     T = float(np.float32(temperature))
     res = oracle.step(x64.reshape(B, L, V), ost, 0, op, temperature=T)
     atie, ytie = _ties(x64, _error_bound(hb, Wb), res.gap.reshape(-1), T)
-    rep = Report()
+    rep = Report(label=f"fused {B}x{L}x{K}x{V}")
     compare_step(g, res, ost, np.ones(B, bool), rep, ctx=f"fused {B}x{L}x{K}x{V}",
                  atie=atie.reshape(B, L), ytie_extra=ytie.reshape(B, L))
     return rep, g, res
@@ -117,9 +117,51 @@ def test_unembed_equals_written_logits_through_streaming_path():
     assert np.array_equal(a["tokens"], b["tokens"])
 
 
+def test_unembed_full_size_all_rows():
+    """One canvas of the fused workload at full size, every row against the oracle: h [256, 2048]
+    x W [2048, 262144], all masked, T=0.8.  Two row blocks, each split over 74 CTAs along the
+    vocabulary (the small-batch schedule).  The oracle's logits are the binary64 product of the
+    numpy generator's h and W, formed 64 rows of W at a time (each chunk is also compared with
+    the device's W); its step runs on all 256 rows, and compare_step checks every row and the
+    selection, counting as ties the rows whose argmax or sample lies within the fp32
+    accumulation bound."""
+    B, L, K, V = 1, 256, 2048, 262144
+    u = eb_synth.cfg4()
+    h = torch.empty((B * L, K), dtype=torch.int16, device="cuda")
+    W = torch.empty((K, V), dtype=torch.int16, device="cuda")
+    synth_dev.unembed_inputs(u.seed, B * L, K, V, u.sigma_w, u.bias, h, W)
+    hb = u.h()[: B * L]
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), hb)
+    gp, op = params_pair(seed=0)
+    c = eb.Canvas(B, L, V, eb.EB_BF16)
+    c.unembed_step(gp, h, W, K, 0, 0.8)
+    g = host_state(c)
+    Wd = W.cpu().numpy().view(np.uint16)
+    del W
+    x64 = np.zeros((B * L, V))
+    absx = np.zeros((B * L, V))
+    hf = oracle.bf16_to_f64(hb)
+    for k0 in range(0, K, 64):
+        kk = np.arange(k0, k0 + 64)
+        Wn = eb_synth.unembed_W_rows(u.seed, kk, V, u.sigma_w, u.bias)
+        assert np.array_equal(Wn, Wd[k0:k0 + 64]), f"generator rows {k0}.."
+        Wf = oracle.bf16_to_f64(Wn)
+        x64 += hf[:, k0:k0 + 64] @ Wf
+        absx += np.abs(hf[:, k0:k0 + 64]) @ np.abs(Wf)
+    del Wd
+    T = float(np.float32(0.8))
+    ost = oracle.State.fresh(B, L)
+    res = oracle.step(x64.reshape(B, L, V), ost, 0, op, temperature=T)
+    atie, ytie = _ties(x64, K * 2.0 ** -23 * absx, res.gap.reshape(-1), T)
+    rep = Report(label="fused 1x256x2048x262144, all rows")
+    compare_step(g, res, ost, np.ones(B, bool), rep, ctx="fused full size", atie=atie.reshape(B, L),
+                 ytie_extra=ytie.reshape(B, L))
+    assert rep.rows == B * L and rep.max_h_err < H_TOL
+    assert rep.row_ties <= 8, rep.line()
+
+
 @pytest.mark.parametrize("B,rows", [
     (4, [0, 1, 127, 128, 300, 511, 640, 1023]),   # the fused workload as the benchmark runs it
-    (1, [0, 1, 100, 127, 128, 200, 254, 255]),    # one canvas: 2 row blocks, 74 CTAs per block
 ])
 def test_unembed_full_size_sampled_rows(B, rows):
     """B canvases x 256 positions, K=2048, V=262144, all masked, T=0.8: device inputs equal

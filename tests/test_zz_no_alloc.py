@@ -59,12 +59,44 @@ def test_noalloc_step_matches_workspace_step_on_two_calls():
         assert (b["committed"] >= 1).all()
 
 
+def test_noalloc_step_at_the_fixed_size_with_the_raw_entropy_pass():
+    """B * L = 8 x 1024 = 8192 positions, the largest batch the fixed array holds, with
+    EB_FLAG_STOP_RAW_ENTROPY, whose second streaming pass keeps its partial states in the
+    upper half of the array: two calls in a row equal eb_sampler_step on a caller-allocated
+    workspace."""
+    B, L, V = 8, 1024, 256
+    cfg = eb_synth.Peaked(B, L, V, "bf16", 3.0, 0.0, 4.0, (0.3,) * B, tuple(range(20, 20 + B)))
+    params = eb.eb_default_params(seed=11, flags=eb.EB_FLAG_STOP_RAW_ENTROPY)
+    rng = np.random.default_rng(8)
+    mask = (rng.random((B, L)) < 0.6).astype(np.uint8)
+    mask[:, 0] = 1
+    ref = eb.Canvas(B, L, V, eb.EB_BF16, mask=mask)
+    fixed = eb.Canvas(B, L, V, eb.EB_BF16, mask=mask)
+    for step in (0, 1):
+        x = torch.empty((B, L, V), dtype=torch.int16, device="cuda")
+        synth_dev.logits(synth_dev.Recipe.of(cfg), step, x)
+        ref.step(params, x, step)
+        _noalloc_step(fixed, params, x, step)
+        a, b = host_state(ref), host_state(fixed)
+        assert np.abs(a["entropy"] - b["entropy"]).max() <= H_TOL, step
+        assert np.abs(a["mean_entropy"] - b["mean_entropy"]).max() <= H_TOL, step
+        for k in ("argmax", "sampled", "selected", "mask", "tokens", "prev_argmax", "status",
+                  "committed"):
+            assert np.array_equal(a[k], b[k]), (step, k)
+
+
 def test_noalloc_step_rejects_batches_above_the_fixed_scratch():
     params = eb.eb_default_params()
     c = eb.Canvas(1, 16, 64, eb.EB_F32)
     with pytest.raises(eb.EbError) as ei:
         # 9 x 1024 positions > 8192: refused before anything is read or launched
         eb.eb_sampler_step_noalloc(params, 9, 1024, 64, eb.EB_F32, c.entropy, 0, 0.0, c.mask,
+                                   c.tokens, c.prev_argmax, c.status, c.steps_taken, c.entropy,
+                                   c.argmax, c.sampled, c.selected, c.committed, c.mean_entropy)
+    assert ei.value.status == eb.EB_ERR_UNSUPPORTED
+    with pytest.raises(eb.EbError) as ei:
+        # one position beyond the fixed size (8193 = 8193 x 1) is refused too
+        eb.eb_sampler_step_noalloc(params, 8193, 1, 64, eb.EB_F32, c.entropy, 0, 0.0, c.mask,
                                    c.tokens, c.prev_argmax, c.status, c.steps_taken, c.entropy,
                                    c.argmax, c.sampled, c.selected, c.committed, c.mean_entropy)
     assert ei.value.status == eb.EB_ERR_UNSUPPORTED

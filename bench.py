@@ -40,7 +40,8 @@ sys.path.insert(0, ROOT)
 METRIC = "EB-sampler steps/s at B×256×262144 bf16; achieved HBM GB/s vs B300 peak"
 B, L, V = 1, 256, 262144
 NSEEDS = 10
-K1_SAMPLES = 60                          # row-statistics launches timed one by one
+K1_SAMPLES = 100                         # row-statistics launches timed one by one
+WARM_SECONDS = 0.5                       # least time of warm-up steps before any timed work
 BYTES_PER_STEP = B * L * V * 2           # algorithmic bytes: every logit read once
 TEMPERATURE = 0.8
 WORKLOAD = ("single EB sampler step: B=1 canvas, L=256 positions, V=262144 bf16 logits "
@@ -302,21 +303,40 @@ def state_ptrs(pool, i):
     return out
 
 
-def k1_sample_times(lib, step_call, n, pool_restore, stream, torch):
-    """CUDA-event durations (ms) of n row-statistics launches, each bracketed by its own pair of
-    events on the launching stream (eb_set_profile_events); every launch is a whole step on a
-    fresh canvas state, restored before the first event.  One synchronisation at the end."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+def k1_graph_samples(lib, one, masks, device, torch, steps=20, replays=5):
+    """CUDA-event durations (ms) of steps x replays row-statistics launches: a CUDA graph of
+    `steps` whole steps (after a restore of their canvas states), each with its row-statistics
+    launch between its own pair of events (eb_set_profile_events during capture), replayed
+    `replays` times; the durations are read after every replay."""
+    pool = state_pool(steps, masks, device)
+    pristine = {k: v.clone() for k, v in pool.items()}
+    ptrs = [state_ptrs(pool, i) for i in range(steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    stream = torch.cuda.current_stream(device)
     for b, e in evs:
         b.record(stream)
-        e.record(stream)          # materialise the CUDA events
+        e.record(stream)          # materialise the CUDA events before capture
     torch.cuda.synchronize()
-    for i, (b, e) in enumerate(evs):
-        pool_restore(i)
-        lib.eb_set_profile_events(b.cuda_event, e.cuda_event)
-        step_call(i)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        graph.capture_begin()
+        for k in pool:
+            pool[k].copy_(pristine[k])
+        csp = torch.cuda.current_stream(device).cuda_stream
+        for j, (b, e) in enumerate(evs):
+            lib.eb_set_profile_events(b.cuda_event, e.cuda_event)
+            one(j, ptrs, csp)
+        graph.capture_end()
     torch.cuda.synchronize()
-    return [b.elapsed_time(e) for b, e in evs]
+    graph.replay()                # untimed
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(replays):
+        graph.replay()
+        torch.cuda.synchronize()
+        ms += [b.elapsed_time(e) for b, e in evs]
+    return ms
 
 
 def sample_stats(ms):
@@ -394,8 +414,15 @@ def run_single(args, lk, device, local, dist, world, timed=True):
             one(j, ptrs, csp)
         graph.capture_end()
     torch.cuda.synchronize()
-    graph.replay()                # one untimed replay after capture
-    torch.cuda.synchronize()
+    # warm-up by time as well as by count: the GPU runs this kernel several per cent slower for
+    # the first few hundred launches of a process, so the graph is replayed for WARM_SECONDS
+    # (at least once) before anything is timed
+    warm_replays = 0
+    t0 = time.perf_counter()
+    while warm_replays < 1 or time.perf_counter() - t0 < WARM_SECONDS:
+        graph.replay()
+        torch.cuda.synchronize()
+        warm_replays += 1
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(dist, local)
@@ -415,21 +442,13 @@ def run_single(args, lk, device, local, dist, world, timed=True):
     if not ((st == 0).all() and (com >= 1).all()):
         raise RuntimeError("timed steps did not run the expected workload")
 
-    # the row-statistics kernel alone: K1_SAMPLES launches, each timed by its own events
-    spool = state_pool(NSEEDS, masks, device)
-    spristine = {k: v.clone() for k, v in spool.items()}
-    sptrs = [state_ptrs(spool, i) for i in range(NSEEDS)]
-
-    def restore(i):
-        j = i % NSEEDS
-        for k in spool:
-            spool[k][j].copy_(spristine[k][j])
-
-    k1_ms = k1_sample_times(lib, lambda i: one(i, sptrs, sp), K1_SAMPLES, restore, stream, torch)
+    # the row-statistics kernel alone: K1_SAMPLES launches inside replays of a timing graph,
+    # each between its own events
+    k1_ms = k1_graph_samples(lib, one, masks, device, torch, steps=20, replays=K1_SAMPLES // 20)
     k1 = sample_stats(k1_ms)
     return {"value": value, "elapsed": elapsed, "slowest": slowest, "K": K, "W": W, "N": N, "R": R,
             "k1": k1, "clocks": clocks.summary(), "bufs": bufs, "masks": masks, "params": params,
-            "stream": stream}
+            "stream": stream, "warm_steps": W + warm_replays * N}
 
 
 def run_ours(args, rank, world, local):
@@ -468,9 +487,11 @@ def run_ours(args, rank, world, local):
             "workload": lk["workload"],
             "B": B, "L": L, "V": V, "logits_dtype": lk["name"], "masked": 128, "temperature": TEMPERATURE,
             "l2": f"10 rotating {lk['bytes'] >> 20} MiB logit buffers ({10 * lk['bytes'] / 2**30:.3g} GiB > 126 MB L2)",
-            "launch": f"CUDA graph of {m['N']} steps (+ one canvas-state restore) replayed {m['R']} times; "
-                      f"row-statistics kernel timed separately over {K1_SAMPLES} launches, each between its "
-                      "own CUDA events",
+            "launch": f"CUDA graph of {m['N']} steps (+ one canvas-state restore) replayed {m['R']} times "
+                      f"after {m['warm_steps']} warm-up steps (at least {WARM_SECONDS} s); row-statistics "
+                      f"kernel timed separately over {K1_SAMPLES} launches: a second graph of 20 steps with "
+                      "CUDA events around each row-statistics launch, replayed "
+                      f"{K1_SAMPLES // 20} times",
             "parallelism": f"replicas x{world}",
         },
         "hbm_gbs_step": lk["bytes"] * K / m["elapsed"] / 1e9,

@@ -49,7 +49,7 @@ namespace ebk {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMaxWeightedRows = 4096;
-constexpr int kK2Threads = 256;
+constexpr int kK2Threads = 512;                     // two threads per canvas row
 constexpr int kMaxL = 1024;
 constexpr int kMaxGrid = 8192;
 constexpr int kWeightUnmasked = 11;                // relative cost of a vector of an unmasked row

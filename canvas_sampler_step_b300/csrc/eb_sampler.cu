@@ -491,7 +491,8 @@ __device__ __forceinline__ unsigned long long k2_row_start(const K2Args &a, long
                       : (unsigned long long)r * (unsigned long long)a.nvec_row;
 }
 
-constexpr int kMergeBatch = 8;   // partial states fetched per round by the selection kernel
+constexpr int kSelGeneral = 4;  // selection flag: more than 32 low-entropy candidates (bits 0-1: halt)
+constexpr int kMergeBatch = 6;   // partial states fetched per round by the selection kernel
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 {
@@ -523,9 +524,12 @@ __device__ __forceinline__ unsigned long long entropy_key(float H, int p)
 // group) slots when k3_g > 0, else the streaming units u.x .. u.y of `rowunits`.  W and G: the
 // streaming partition's total weight and unit count (a unit whose weight range is empty wrote
 // nothing, only when W < G).
+// `half` (0 or 1): this thread merges the first or the second half of the row's slots (the two
+// threads of a row combine their halves in that order afterwards).
 __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *partials, const int2 *rowunits,
                                              unsigned long long W, unsigned long long G, long long r, float c,
-                                             RowState &st, int &flags)
+                                             int half, RowState &st, int &flags, const int2 *local_units = nullptr,
+                                             int p = 0)
 {
     long long base, stride;
     int n;
@@ -535,20 +539,22 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
         stride = 128;
         n = a.k3_groups * a.k3_g;
     } else {
-        const int2 u = rowunits[r];
+        const int2 u = local_units ? local_units[p] : rowunits[r];
         base = r + u.x;
         stride = 1;
         n = u.y - u.x + 1;
     }
+    const int h = (n + 1) >> 1;
+    const int lo = half ? h : 0, hi = half ? n : h;
     // loads in batches of kMergeBatch independent requests, merged in slot order
-    for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
+    for (int i0 = lo; i0 < hi; i0 += kMergeBatch) {
         Partial q[kMergeBatch];
 #pragma unroll
         for (int k = 0; k < kMergeBatch; ++k)
-            if (i0 + k < n) q[k] = partials[base + (long long)(i0 + k) * stride];
+            if (i0 + k < hi) q[k] = partials[base + (long long)(i0 + k) * stride];
 #pragma unroll
         for (int k = 0; k < kMergeBatch; ++k) {
-            if (i0 + k >= n) break;
+            if (i0 + k >= hi) break;
             if (a.k3_g == 0 && W < G) {
                 const unsigned long long cu = (unsigned long long)(base - r + i0 + k);
                 if (cu * W / G >= (cu + 1) * W / G) continue;
@@ -556,6 +562,23 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
             merge_state(st, q[k].xm, q[k].S, q[k].T2, q[k].ai, q[k].best, q[k].bi, c);
             flags |= q[k].flags;
         }
+    }
+}
+
+// The two threads of a row (lanes 2k, 2k + 1): the even one merges the odd one's state into
+// its own, the even one's half of the slots first.
+__device__ __forceinline__ void pair_combine(RowState &st, int &flags, float c)
+{
+    const float xm = __shfl_xor_sync(0xFFFFFFFFu, st.xm, 1);
+    const float S = __shfl_xor_sync(0xFFFFFFFFu, st.S, 1);
+    const float T2 = __shfl_xor_sync(0xFFFFFFFFu, st.T2, 1);
+    const int ai = __shfl_xor_sync(0xFFFFFFFFu, st.ai, 1);
+    const float best = __shfl_xor_sync(0xFFFFFFFFu, st.best, 1);
+    const int bi = __shfl_xor_sync(0xFFFFFFFFu, st.bi, 1);
+    const int of = __shfl_xor_sync(0xFFFFFFFFu, flags, 1);
+    if ((threadIdx.x & 1) == 0) {
+        merge_state(st, xm, S, T2, ai, best, bi, c);
+        flags |= of;
     }
 }
 
@@ -572,8 +595,13 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     __shared__ uint8_t Acc[kMaxL];               // accepted at this step
     __shared__ unsigned long long red_sum[kK2Threads / 32];
     __shared__ unsigned long long red_min[kK2Threads / 32];
-    __shared__ unsigned long long small_total;
-    __shared__ int n_masked, n_small, n_gather, n_committed, bad_flags, all_small;
+    __shared__ int4 red_cnt[kK2Threads / 32];   // per warp: masked, small, bad flags, unstable
+    __shared__ uint32_t wtot[kK2Threads / 32];
+    // per row: first and last partition unit (phase 1 only; shares the general sort's scan buffer)
+    int2 *Ru = reinterpret_cast<int2 *>(scanbuf);
+    __shared__ int n_gather, n_acc, sel_status, sel_committed, sel_flag, sel_stop, sel_ns, sel_nm, sel_cap;
+    __shared__ float sel_mean;
+    __shared__ unsigned long long sel_bigmin;
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -582,15 +610,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     // the canvas's own step and c under continuous batching, else the launch's
     const int step = a.canvas_step ? a.canvas_step[b] : a.step;
     const float cb = a.canvas_c ? a.canvas_c[b] : a.c;
-    if (tid == 0) {
-        n_masked = 0;
-        n_small = 0;
-        n_gather = 0;
-        n_committed = 0;
-        bad_flags = 0;
-        all_small = 1;
-        small_total = 0;
-    }
+    if (tid == 0) n_gather = 0;
     const long long rowbase = (long long)b * L;
     // launched as a programmatic dependent of the row-statistics kernel: the mask and the
     // previous argmax are not written by it, so they load while it drains; wait for its
@@ -599,8 +619,44 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         Ms[p] = a.mask[rowbase + p] ? 1 : 0;
         Pv[p] = a.prev_argmax[rowbase + p];
     }
+    // One canvas on the weighted partition: the row statistics' partition is a function of this
+    // canvas's mask alone, so each row's first and last partition unit are computed here, before
+    // the wait, instead of being read after it.  Unit g covers weight [g W / G, (g + 1) W / G),
+    // so the unit holding weight position x is ((x + 1) G - 1) / W.
+    const bool local = a.weighted && a.k3_g == 0 && a.rows == L && !a.canvas_step;
+    unsigned long long Wloc = 0;
+    if (local) {
+        __syncthreads();                          // Ms complete
+        const uint32_t wm = (uint32_t)a.nvec_row * (uint32_t)kWeightMasked;
+        const uint32_t wu = (uint32_t)a.nvec_row * (uint32_t)kWeightUnmasked;
+        // exclusive scan of the row weights, two rows per thread (L <= 1024 = 2 x 512)
+        const int p0 = 2 * tid;
+        const uint32_t w0 = p0 < L ? (Ms[p0] ? wm : wu) : 0u;
+        const uint32_t w1 = p0 + 1 < L ? (Ms[p0 + 1] ? wm : wu) : 0u;
+        const uint32_t mine = w0 + w1;
+        uint32_t incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) wtot[warp] = incl;
+        __syncthreads();
+        uint32_t before = 0, total = 0;
+        for (int w = 0; w < kK2Threads / 32; ++w) {
+            const uint32_t t = wtot[w];
+            if (w < warp) before += t;
+            total += t;
+        }
+        const unsigned long long Wt = total, Gt = (unsigned long long)a.G;
+        const unsigned long long x0 = before + incl - mine;      // weight before row p0
+        auto unit = [&](unsigned long long x) { return (int)(((x + 1ull) * Gt - 1ull) / Wt); };
+        if (p0 < L) Ru[p0] = make_int2(unit(x0), unit(x0 + w0 - 1ull));
+        if (p0 + 1 < L) Ru[p0 + 1] = make_int2(unit(x0 + w0), unit(x0 + w0 + w1 - 1ull));
+        Wloc = Wt;
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const unsigned long long W = k2_row_start(a, a.rows);
+    const unsigned long long W = local ? Wloc : k2_row_start(a, a.rows);
     const unsigned long long G = (unsigned long long)a.G;
     const unsigned long long Wr = !a.raw_partials ? 0ull
                                   : a.raw_weighted ? (unsigned long long)a.raw_prefix[a.rows]
@@ -608,14 +664,28 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     const unsigned long long Gr = (unsigned long long)a.raw_G;
     __syncthreads();
 
-    // 1. merge each row's partials (ascending CTA) -> H, A, Y
+    // 1. merge each row's partials (ascending unit) -> H, A, Y.  Two threads per row: each merges
+    // half of the row's slots, then the first half takes the second's state (a fixed order, so
+    // the result does not depend on timing) and carries on alone.
     unsigned long long my_sum = 0, my_bigmin = ~0ull;
     int my_unstable = 0, my_bad = 0, my_masked = 0, my_small = 0;
-    for (int p = tid; p < L; p += blockDim.x) {
-        const long long r = rowbase + p;
+    const int half = tid & 1;
+    for (int p0 = 0; p0 < L; p0 += (int)(blockDim.x >> 1)) {
+        const int p = p0 + (tid >> 1);
+        const bool row_here = p < L;             // the same for both threads of a pair
+        const long long r = rowbase + (row_here ? p : 0);
         RowState st = empty_state();
         int flags = 0;
-        k2_merge_row(a, a.partials, a.rowunits, W, G, r, cb, st, flags);
+        if (row_here) k2_merge_row(a, a.partials, a.rowunits, W, G, r, cb, half, st, flags, local ? Ru : nullptr, p);
+        pair_combine(st, flags, cb);
+        RowState sr = empty_state();
+        int rflags = 0;
+        if (a.raw_partials) {
+            // EB_FLAG_STOP_RAW_ENTROPY: the raw-logit (T = 1) pass's partial states, same scheme
+            if (row_here) k2_merge_row(a, a.raw_partials, a.raw_rowunits, Wr, Gr, r, kLog2e, half, sr, rflags);
+            pair_combine(sr, rflags, kLog2e);
+        }
+        if (!row_here || half) continue;
         float H = kLn2 * (log2f(st.S) - st.T2 / st.S);
         if (H < 0.0f) H = 0.0f;                  // rounding below zero (NaN passes through)
         H = H + 0.0f;                            // -0 -> +0 so the key bits order correctly
@@ -629,9 +699,6 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         unsigned long long hstat = hq;           // the entropy the stop rule sums
         if (a.raw_partials) {
             // EB_FLAG_STOP_RAW_ENTROPY: the entropy of the raw logits (T = 1), same fixed point
-            RowState sr = empty_state();
-            int rflags = 0;
-            k2_merge_row(a, a.raw_partials, a.raw_rowunits, Wr, Gr, r, kLog2e, sr, rflags);
             float Hr = kLn2 * (log2f(sr.S) - sr.T2 / sr.S);
             if (Hr < 0.0f) Hr = 0.0f;
             if (!isfinite(Hr) || (rflags & kPartialNonfinite)) my_bad |= 1;
@@ -661,29 +728,120 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
             }
         }
     }
-    const unsigned long long ws = warp_sum_u64(my_sum);
-    const unsigned long long wm = warp_min_u64(my_bigmin);
-    if (lane == 0) {
-        red_sum[warp] = ws;
-        red_min[warp] = wm;
+    // the canvas statistics: warp reductions into one shared slot per warp and one barrier;
+    // then warp 0 alone reduces the slots, takes the stop decision and, with at most 32
+    // low-entropy candidates, the whole selection, while the other warps wait at the next barrier
+    {
+        const unsigned long long ws = warp_sum_u64(my_sum);
+        const unsigned long long wm = warp_min_u64(my_bigmin);
+        const int wcnt_m = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)my_masked);
+        const int wcnt_s = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)my_small);
+        const int wbad = (int)__reduce_or_sync(0xFFFFFFFFu, (unsigned)my_bad);
+        const int wuns = (int)__reduce_or_sync(0xFFFFFFFFu, (unsigned)my_unstable);
+        if (lane == 0) {
+            red_sum[warp] = ws;
+            red_min[warp] = wm;
+            red_cnt[warp] = make_int4(wcnt_m, wcnt_s, wbad, wuns);
+        }
     }
-    if (my_masked) atomicAdd(&n_masked, my_masked);
-    if (my_small) atomicAdd(&n_small, my_small);
-    if (my_bad) atomicOr(&bad_flags, my_bad);
-    const bool stable = __syncthreads_or(my_unstable) == 0;
-    unsigned long long sumq = 0, bigmin = ~0ull;
-    for (int w = 0; w < kK2Threads / 32; ++w) {
-        sumq += red_sum[w];
-        bigmin = red_min[w] < bigmin ? red_min[w] : bigmin;
+    __syncthreads();
+    constexpr int kNW = kK2Threads / 32;
+    if (warp == 0) {
+        const unsigned long long sumq = warp_sum_u64(lane < kNW ? red_sum[lane] : 0ull);
+        const unsigned long long bigmin = warp_min_u64(lane < kNW ? red_min[lane] : ~0ull);
+        const int4 cw = lane < kNW ? red_cnt[lane] : make_int4(0, 0, 0, 0);
+        const int nm = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cw.x);
+        const int ns = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cw.y);
+        const int badf = (int)__reduce_or_sync(0xFFFFFFFFu, (unsigned)cw.z);
+        const bool stable = __reduce_or_sync(0xFFFFFFFFu, (unsigned)cw.w) == 0u;
+        const int nstat = a.stop_masked_only ? nm : L;
+        const long long stop_q =
+            a.stop_masked_only ? (long long)ceil(a.stop_entropy * (double)nstat * 1099511627776.0) : a.stop_q;
+        const bool stop = !badf && step >= 1 && stable && nstat > 0 && (long long)sumq < stop_q;
+        const bool at_cap = step >= a.max_steps - 1;
+        if (lane == 0) {
+            sel_mean = nstat > 0 ? (float)sumq * 9.094947017729282e-13f / (float)nstat : NAN;   // 2^-40
+            sel_flag = badf ? badf : 0;
+            sel_stop = stop ? 1 : 0;
+        }
+        if (badf) {
+            // nothing to select
+        } else if (stop) {
+            // adaptive stop: every still-masked position takes its argmax (in the commit pass)
+            if (lane == 0) {
+                sel_status = EB_STOP_ADAPTIVE;
+                sel_committed = nm;
+            }
+        } else if (nm == 0) {
+            if (lane == 0) {
+                sel_status = EB_STOP_COMPLETE;
+                sel_committed = 0;
+            }
+        } else if (ns <= 32) {
+            // gather the low-entropy candidates in position order by ballot, sort them, accept
+            // the prefix, then the lowest position above the bound if the prefix allows
+            int cnt = 0;
+            for (int p0 = 0; p0 < L; p0 += 32) {
+                const int p = p0 + lane;
+                const bool cand = p < L && Ms[p] && (long long)Hq[p] <= a.bound_q;
+                const unsigned bal = __ballot_sync(0xFFFFFFFFu, cand);
+                if (cand) keys[cnt + __popc(bal & ((1u << lane) - 1u))] = entropy_key(Hf[p], p);
+                cnt += __popc(bal);
+            }
+            __syncwarp();
+            unsigned long long k = lane < ns ? keys[lane] : ~0ull;
+            // bitonic sort of 32 keys across the warp, ascending
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, k, stride);
+                    const bool up = (lane & size) == 0;
+                    const bool lower = (lane & stride) == 0;
+                    const unsigned long long lo = o < k ? o : k, hi = o < k ? k : o;
+                    k = (lower == up) ? lo : hi;
+                }
+            }
+            const int pos = (int)(k & 0xFFFFFFFFu);
+            const unsigned long long h = lane < ns ? Hq[pos] : 0ull;
+            unsigned long long incl = h;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const unsigned long long excl = incl - h;
+            const bool acc = lane < ns && (lane == 0 || (long long)excl <= a.bound_q);
+            if (acc) Acc[pos] = 1;
+            const unsigned acc_mask = __ballot_sync(0xFFFFFFFFu, acc);
+            const unsigned ok_mask = __ballot_sync(0xFFFFFFFFu, acc || lane >= ns);
+            const unsigned long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (lane == 0) {
+                int nacc = __popc(acc_mask);
+                // sorted index ns: the lowest-entropy position above the bound
+                if (bigmin != ~0ull && (ns == 0 || (ok_mask == 0xFFFFFFFFu && (long long)tot <= a.bound_q))) {
+                    Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
+                    ++nacc;
+                }
+                const int left = nm - nacc;
+                sel_status = left == 0 ? EB_STOP_COMPLETE : (at_cap ? EB_STOP_CAP : EB_RUNNING);
+                sel_committed = nacc + (left > 0 && at_cap ? left : 0);
+            }
+        } else if (lane == 0) {
+            sel_flag = kSelGeneral;          // more than 32 candidates: the whole CTA sorts them
+            sel_ns = ns;
+            sel_nm = nm;
+            sel_bigmin = bigmin;
+            sel_cap = at_cap ? 1 : 0;
+        }
     }
-    const int nm = n_masked, ns = n_small;
-    const int nstat = a.stop_masked_only ? nm : L;
-    const float mean = nstat > 0 ? (float)((double)sumq / 1099511627776.0 / (double)nstat) : NAN;
-    const long long stop_q =
-        a.stop_masked_only ? (long long)ceil(a.stop_entropy * (double)nstat * 1099511627776.0) : a.stop_q;
-    if (bad_flags) {
+    __syncthreads();
+    const int flag = sel_flag;
+    const bool stop = sel_stop != 0;
+    if (flag & 3) {
+        // non-finite logits or a wait that gave up: the canvas halts with nothing committed
         if (tid == 0) {
-            a.status[b] = ((bad_flags & 1) ? EB_STATUS_NONFINITE : 0) | ((bad_flags & 2) ? EB_STATUS_TIMEOUT : 0);
+            a.status[b] = ((flag & 1) ? EB_STATUS_NONFINITE : 0) | ((flag & 2) ? EB_STATUS_TIMEOUT : 0);
             if (a.steps_taken) a.steps_taken[b] = step + 1;
             if (a.committed) a.committed[b] = 0;
             if (a.mean_entropy) a.mean_entropy[b] = NAN;
@@ -691,120 +849,83 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         for (int p = tid; p < L; p += blockDim.x) a.selected[rowbase + p] = 0;
         return;
     }
-    const bool stop = step >= 1 && stable && nstat > 0 && (long long)sumq < stop_q;
-
-    if (stop) {
-        // adaptive stop: every still-masked position takes its argmax
-        for (int p = tid; p < L; p += blockDim.x) Acc[p] = Ms[p];
-    } else if (nm > 0) {
-        // 2. gather the low-entropy candidates (their own counter: n_small, which every
-        // thread read above, must not change under a lagging warp)
+    if (flag == kSelGeneral) {
+        const int ns = sel_ns, nm = sel_nm;
+        const unsigned long long bigmin = sel_bigmin;
+        const bool at_cap = sel_cap != 0;
+        // general path: the candidates gathered by atomics, a bitonic sort in shared memory
+        if (tid == 0) n_acc = 0;
         for (int p = tid; p < L; p += blockDim.x) {
             if (Ms[p] && (long long)Hq[p] <= a.bound_q) {
                 const int i = atomicAdd(&n_gather, 1);
                 keys[i] = entropy_key(Hf[p], p);
             }
         }
+        int n2 = 1;
+        while (n2 < ns) n2 <<= 1;
+        for (int i = ns + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
         __syncthreads();
-        if (ns <= 32) {
-            if (warp == 0) {
-                unsigned long long k = lane < ns ? keys[lane] : ~0ull;
-                // bitonic sort of 32 keys across the warp, ascending
-#pragma unroll
-                for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, k, stride);
-                        const bool up = (lane & size) == 0;
-                        const bool lower = (lane & stride) == 0;
-                        const unsigned long long lo = o < k ? o : k, hi = o < k ? k : o;
-                        k = (lower == up) ? lo : hi;
-                    }
-                }
-                const int pos = (int)(k & 0xFFFFFFFFu);
-                const unsigned long long h = lane < ns ? Hq[pos] : 0ull;
-                unsigned long long incl = h;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-                    if (lane >= off) incl += o;
-                }
-                const unsigned long long excl = incl - h;
-                const bool acc = lane < ns && (lane == 0 || (long long)excl <= a.bound_q);
-                if (acc) Acc[pos] = 1;
-                const unsigned ok_mask = __ballot_sync(0xFFFFFFFFu, acc || lane >= ns);
-                const unsigned long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-                if (lane == 0) {
-                    all_small = ok_mask == 0xFFFFFFFFu ? 1 : 0;
-                    small_total = tot;
-                }
-            }
-        } else {
-            // general path: bitonic sort of the ns candidates in shared memory
-            int n2 = 1;
-            while (n2 < ns) n2 <<= 1;
-            for (int i = ns + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
-            __syncthreads();
-            for (int size = 2; size <= n2; size <<= 1) {
-                for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                    for (int i = tid; i < n2; i += blockDim.x) {
-                        const int ixj = i ^ stride;
-                        if (ixj > i) {
-                            const unsigned long long x = keys[i], y = keys[ixj];
-                            const bool up = (i & size) == 0;
-                            if ((x > y) == up) {
-                                keys[i] = y;
-                                keys[ixj] = x;
-                            }
+        for (int size = 2; size <= n2; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < n2; i += blockDim.x) {
+                    const int ixj = i ^ stride;
+                    if (ixj > i) {
+                        const unsigned long long x = keys[i], y = keys[ixj];
+                        const bool up = (i & size) == 0;
+                        if ((x > y) == up) {
+                            keys[i] = y;
+                            keys[ixj] = x;
                         }
                     }
-                    __syncthreads();
                 }
+                __syncthreads();
             }
-            // inclusive scan of the sorted fixed-point entropies (Hillis-Steele)
-            for (int i = tid; i < n2; i += blockDim.x)
-                scanbuf[i] = i < ns ? Hq[(int)(keys[i] & 0xFFFFFFFFu)] : 0ull;
+        }
+        // inclusive scan of the sorted fixed-point entropies (Hillis-Steele)
+        for (int i = tid; i < n2; i += blockDim.x)
+            scanbuf[i] = i < ns ? Hq[(int)(keys[i] & 0xFFFFFFFFu)] : 0ull;
+        __syncthreads();
+        for (int off = 1; off < n2; off <<= 1) {
+            unsigned long long add[kMaxL / kK2Threads];
+            int q = 0;
+            for (int i = tid; i < n2; i += blockDim.x, ++q) add[q] = i >= off ? scanbuf[i - off] : 0ull;
             __syncthreads();
-            for (int off = 1; off < n2; off <<= 1) {
-                unsigned long long add[kMaxL / kK2Threads];
-                int q = 0;
-                for (int i = tid; i < n2; i += blockDim.x, ++q) add[q] = i >= off ? scanbuf[i - off] : 0ull;
-                __syncthreads();
-                q = 0;
-                for (int i = tid; i < n2; i += blockDim.x, ++q) scanbuf[i] += add[q];
-                __syncthreads();
+            q = 0;
+            for (int i = tid; i < n2; i += blockDim.x, ++q) scanbuf[i] += add[q];
+            __syncthreads();
+        }
+        int my_acc = 0, my_rej = 0;
+        for (int i = tid; i < ns; i += blockDim.x) {
+            const unsigned long long excl = i == 0 ? 0ull : scanbuf[i - 1];
+            if (i == 0 || (long long)excl <= a.bound_q) {
+                Acc[(int)(keys[i] & 0xFFFFFFFFu)] = 1;
+                ++my_acc;
+            } else {
+                my_rej = 1;
             }
-            int my_rej = 0;
-            for (int i = tid; i < ns; i += blockDim.x) {
-                const unsigned long long excl = i == 0 ? 0ull : scanbuf[i - 1];
-                if (i == 0 || (long long)excl <= a.bound_q) Acc[(int)(keys[i] & 0xFFFFFFFFu)] = 1;
-                else my_rej = 1;
+        }
+        if (my_acc) atomicAdd(&n_acc, my_acc);
+        const bool all_acc = __syncthreads_or(my_rej) == 0;
+        if (tid == 0) {
+            int nacc = n_acc;
+            if (bigmin != ~0ull && all_acc && (long long)scanbuf[ns - 1] <= a.bound_q) {
+                Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
+                ++nacc;
             }
-            if (my_rej) all_small = 0;
-            if (tid == 0) small_total = scanbuf[ns - 1];
+            const int left = nm - nacc;
+            sel_status = left == 0 ? EB_STOP_COMPLETE : (at_cap ? EB_STOP_CAP : EB_RUNNING);
+            sel_committed = nacc + (left > 0 && at_cap ? left : 0);
         }
         __syncthreads();
-        // sorted index ns: the lowest-entropy position above the bound
-        if (tid == 0 && bigmin != ~0ull) {
-            if (ns == 0 || (all_small && (long long)small_total <= a.bound_q))
-                Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
-        }
     }
-    __syncthreads();
 
     // 3. commit, re-mask, complete / cap
-    int my_left = 0;
-    for (int p = tid; p < L; p += blockDim.x) my_left |= (Ms[p] && !Acc[p]) ? 1 : 0;
-    const bool any_left = __syncthreads_or(my_left) != 0;
-    int new_status = EB_RUNNING;
-    if (stop) new_status = EB_STOP_ADAPTIVE;
-    else if (!any_left) new_status = EB_STOP_COMPLETE;
-    else if (step >= a.max_steps - 1) new_status = EB_STOP_CAP;
-    int my_commit = 0;
+    const int new_status = sel_status;
+    const float mean = sel_mean;
     for (int p = tid; p < L; p += blockDim.x) {
         const long long r = rowbase + p;
         uint8_t sel = 0;
-        if (Acc[p]) {
+        if (stop ? Ms[p] : Acc[p]) {
             a.tokens[r] = (stop && !a.finalize_sampled) ? As[p] : Ys[p];
             a.mask[r] = 0;
             sel = 1;
@@ -813,14 +934,11 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
             a.mask[r] = 0;
             sel = 1;
         }
-        my_commit += sel;
         a.selected[r] = sel;
         a.prev_argmax[r] = As[p];
     }
-    if (my_commit) atomicAdd(&n_committed, my_commit);
-    __syncthreads();
     if (tid == 0) {
-        const int committed = n_committed;
+        const int committed = sel_committed;
         if (new_status != EB_RUNNING) {
             a.status[b] = new_status;
             if (a.steps_taken) a.steps_taken[b] = step + 1;

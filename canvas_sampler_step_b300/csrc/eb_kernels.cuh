@@ -179,13 +179,6 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return r;
 }
 
-__device__ __forceinline__ float min3(float a, float b, float c)
-{
-    float r;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 // Packed pairs of binary32 values in one 64-bit register (Blackwell f32x2 arithmetic: one
 // instruction per two lanes' worth of FADD / FFMA / FMUL).
 typedef unsigned long long f32x2;
@@ -973,15 +966,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
         if (done) return true;
     }
     return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
 }
 
 __device__ __forceinline__ void consumer_sync()

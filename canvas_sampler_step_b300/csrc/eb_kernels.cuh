@@ -339,6 +339,22 @@ __device__ __forceinline__ float gumbel_score_estimate(float x, uint32_t w, floa
     return fmaf(-lg2_approx(E), kLn2, x * invT);
 }
 
+// The same estimate without a branch (both forms of -ln u computed, one selected), for the
+// seed of a segment, where every entry of a batch takes it.
+__device__ __forceinline__ float gumbel_score_estimate_sel(float x, uint32_t w, float invT)
+{
+    const float delta = (2.0f - u_prime(w)) - 5.9604644775390625e-8f;
+    const float Es = delta * fmaf(delta, fmaf(delta, 0.333333343f, 0.5f), 1.0f);
+    const float El = -lg2_approx(1.0f - delta) * kLn2;
+    return fmaf(-lg2_approx(delta < 0.03125f ? Es : El), kLn2, x * invT);
+}
+
+// The margin that covers the estimate's error and the rounding of either score near s.
+__device__ __forceinline__ float estimate_margin(float s)
+{
+    return fmaf(fabsf(s), 9.5367431640625e-7f, 1.0e-4f);
+}
+
 __device__ __forceinline__ float cand_scale(float xm, float best, float c)
 {
     return ex2(fmaf(xm, c, -best * kLog2e)) * kCandSlack;
@@ -546,24 +562,17 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
     return best;
 }
 
-// The best exact score over the warp's lanes of one entry each (x, w, index idx): the seed of a
-// segment's best score.  Out of line: it runs once per segment.
-__device__ __noinline__ GumbelBest gumbel_seed(float x, uint32_t w, float invT, int idx)
-{
-    float sb = gumbel_score(x, w, invT);
-    if (sb != sb) sb = -INFINITY;
-    warp_best(sb, idx);
-    return GumbelBest{sb, sb == -INFINITY ? -1 : idx};
-}
-
 // The streaming kernel's exact pass over a group of N logits (entries v0 ..) of a lane whose
 // candidate test passed: every entry with bits(u' + e K) & kCandBit takes a score estimate, and
-// only an entry whose estimate comes within a margin of the best score takes the exact score
-// (the margin, 1e-4 + |best| 2^-20, exceeds the estimate's error and the rounding of either
-// score).  2^t is recomputed from the logits exactly as the batch computed it.
+// only an entry whose estimate comes within a margin of the reference takes the exact score.
+// The reference is the larger of the best score and floor_score, a lower bound of the
+// segment's best score (its seed threshold); the margin, 1e-4 + |reference| 2^-20, exceeds the
+// estimate's error and the rounding of either score.  2^t is recomputed from the logits exactly
+// as the batch computed it.
 template <int N>
 __device__ __noinline__ GumbelBest gumbel_exact_filtered(float4 xa, float4 xb, uint4 wa, uint4 wb, uint32_t v0,
-                                                         float c, float invT, float nb, float K, GumbelBest best)
+                                                         float c, float invT, float nb, float K, float floor_score,
+                                                         GumbelBest best)
 {
     const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
     const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
@@ -572,8 +581,8 @@ __device__ __noinline__ GumbelBest gumbel_exact_filtered(float4 xa, float4 xb, u
         const float e = ex2(fmaf(x[j], c, nb));
         if (__float_as_uint(fmaf(e, K, u_prime(w[j]))) & kCandBit) {
             const float est = gumbel_score_estimate(x[j], w[j], invT);
-            const float margin = fmaf(fabsf(best.score), 9.5367431640625e-7f, 1.0e-4f);
-            if (!(est < best.score - margin)) {
+            const float ref = fmaxf(best.score, floor_score);
+            if (!(est < ref - estimate_margin(ref))) {
                 const float score = gumbel_score(x[j], w[j], invT);
                 const int idx = (int)(v0 + (uint32_t)j);
                 if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
@@ -784,7 +793,7 @@ __device__ __forceinline__ float vec_max(const float (&x)[N])
 template <int VEC, int U, bool MASKED>
 __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0, const K1Args &a, const RowCtx &rc,
                                               const PhiloxRow &ph, f32x2 c2, RowState &st, PackedSums &q,
-                                              float &nb, f32x2 &nb2, float &K)
+                                              float &nb, f32x2 &nb2, float &K, float &bt)
 {
     constexpr int N = U * VEC;
     float x[N];
@@ -827,17 +836,7 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
         st.xm = wm;
         nb = -wm * rc.c;
         nb2 = pk2(nb, nb);
-        if constexpr (MASKED) {
-            if (st.best == -INFINITY) {
-                // the segment's first batch: every lane's first entry seeds the best score, so
-                // that the candidate test has a finite score to beat from the start
-                const uint32_t w0 = philox_row_block(jv0 * (uint32_t)(VEC / 4), ph, a.keys).x;
-                const GumbelBest g = gumbel_seed(x[0], w0, rc.invT, (int)(jv0 * (uint32_t)VEC));
-                st.best = g.score;
-                st.bi = g.idx;
-            }
-            K = cand_scale(st.xm, st.best, rc.c);
-        }
+        if constexpr (MASKED) K = cand_scale(st.xm, fmaxf(st.best, bt), rc.c);
     }
     // the Philox words of the batch's entries (masked rows), drawn after the vote so that they
     // are not live across its branch; their chains interleave with the exponentials below
@@ -873,6 +872,17 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
         }
     }
     if constexpr (MASKED) {
+        if (bt == -INFINITY) {
+            // the segment's first batch: the largest score estimate of all its entries, less the
+            // estimate's margin, is a lower bound of the segment's best score.  With it as the
+            // threshold, only entries near that maximum pass the candidate test below.
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < N; ++i) m = fmaxf(m, gumbel_score_estimate_sel(x[i], w[i], rc.invT));
+            m = key_value(__reduce_max_sync(0xFFFFFFFFu, order_key(m)));
+            bt = m == INFINITY ? m : m - estimate_margin(m);
+            K = cand_scale(st.xm, fmaxf(st.best, bt), rc.c);
+        }
         // candidate test of two entries at a time: u' + 2^t K on packed FMA, the results' bits
         // or-ed together; bit 30 of the or is set iff some entry's sum reached 2
         uint32_t cacc[U];
@@ -914,13 +924,13 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
                                                  : make_uint4(0u, 0u, 0u, 0u);
                         const GumbelBest g = gumbel_exact_filtered<G8>(
                             xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC + (uint32_t)(G8 * h), rc.c, rc.invT,
-                            nb, K, GumbelBest{st.best, st.bi});
+                            nb, K, bt, GumbelBest{st.best, st.bi});
                         st.best = g.score;
                         st.bi = g.idx;
                     }
                 }
             warp_best(st.best, st.bi);
-            K = cand_scale(st.xm, st.best, rc.c);
+            K = cand_scale(st.xm, fmaxf(st.best, bt), rc.c);
         }
     }
 }

@@ -292,7 +292,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 template <int VEC, int U, bool MASKED>
 __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t nfull,
                                               const RowCtx &rc, const PhiloxRow &ph, f32x2 c2, RowState &st,
-                                              PackedSums &q, float &nb, f32x2 &nb2, float &K, uint32_t sbase)
+                                              PackedSums &q, float &nb, f32x2 &nb2, float &K, float &bt,
+                                              uint32_t sbase)
 {
     constexpr uint32_t kBatch = 32u * U;
     constexpr uint32_t kSlotStride = kDirectThreads * 16u;
@@ -329,7 +330,7 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r[u] = lds128(sbase + off + (uint32_t)u * kSlotStride);
-        consume_batch<VEC, U, MASKED>(r, jv, a, rc, ph, c2, st, q, nb, nb2, K);
+        consume_batch<VEC, U, MASKED>(r, jv, a, rc, ph, c2, st, q, nb, nb2, K, bt);
         off = (off + kDepthStride) & (kRing - 1);
         jv += kBatch;
     }
@@ -354,12 +355,13 @@ __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src,
     const uint32_t nfull = (j1 - j0) / kBatch;
     const uint32_t jf = j0 + nfull * kBatch;
     const uint32_t sbase = smem_addr(stage) + threadIdx.x * 16u;
+    float bt = -INFINITY;                  // the seed threshold (a lower bound of the best score)
     if (nfull > 0) {
         if (gumbel) {
             const PhiloxRow ph = philox_row(rc.p, rc.step, rc.sw, a.keys);
-            async_batches<VEC, U, true>(a, src, j0, nfull, rc, ph, c2, st, q, nb, nb2, K, sbase);
+            async_batches<VEC, U, true>(a, src, j0, nfull, rc, ph, c2, st, q, nb, nb2, K, bt, sbase);
         } else {
-            async_batches<VEC, U, false>(a, src, j0, nfull, rc, PhiloxRow{}, c2, st, q, nb, nb2, K, sbase);
+            async_batches<VEC, U, false>(a, src, j0, nfull, rc, PhiloxRow{}, c2, st, q, nb, nb2, K, bt, sbase);
         }
     }
     if constexpr (VEC == 16) {

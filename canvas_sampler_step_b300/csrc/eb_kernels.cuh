@@ -328,19 +328,9 @@ __device__ __forceinline__ float gumbel_score(float x, uint32_t w, float invT)
 }
 
 // A cheap estimate of the same score, within 2e-5 of it: ln E from lg2.approx, and -ln u from
-// its series for 1 - u < 2^-5 (relative error < 8e-6), else from lg2.approx of u.
-__device__ __forceinline__ float gumbel_score_estimate(float x, uint32_t w, float invT)
-{
-    const float up = u_prime(w);
-    const float delta = (2.0f - up) - 5.9604644775390625e-8f;
-    float E;
-    if (delta < 0.03125f) E = delta * fmaf(delta, fmaf(delta, 0.333333343f, 0.5f), 1.0f);
-    else E = -lg2_approx(1.0f - delta) * kLn2;
-    return fmaf(-lg2_approx(E), kLn2, x * invT);
-}
-
-// The same estimate without a branch (both forms of -ln u computed, one selected), for the
-// seed of a segment, where every entry of a batch takes it.
+// its series for 1 - u < 2^-5 (relative error < 8e-6), else from lg2.approx of u.  Both forms
+// are computed and one is selected, so that the seed of a segment, where every entry of a batch
+// takes it, runs without a branch.
 __device__ __forceinline__ float gumbel_score_estimate_sel(float x, uint32_t w, float invT)
 {
     const float delta = (2.0f - u_prime(w)) - 5.9604644775390625e-8f;
@@ -563,31 +553,36 @@ __device__ __noinline__ GumbelBest gumbel_exact_group(float4 xa, float4 xb, uint
 }
 
 // The streaming kernel's exact pass over a group of N logits (entries v0 ..) of a lane whose
-// candidate test passed: every entry with bits(u' + e K) & kCandBit takes a score estimate, and
-// only an entry whose estimate comes within a margin of the reference takes the exact score.
-// The reference is the larger of the best score and floor_score, a lower bound of the
-// segment's best score (its seed threshold); the margin, 1e-4 + |reference| 2^-20, exceeds the
-// estimate's error and the rounding of either score.  2^t is recomputed from the logits exactly
-// as the batch computed it.
+// candidate test passed.  The group's entries are tested again one by one (2^t recomputed from
+// the logits exactly as the batch computed it) into a bit mask, and only the flagged entries,
+// usually one, take the exact score, in a loop over the mask: the code stays small.
 template <int N>
-__device__ __noinline__ GumbelBest gumbel_exact_filtered(float4 xa, float4 xb, uint4 wa, uint4 wb, uint32_t v0,
-                                                         float c, float invT, float nb, float K, float floor_score,
-                                                         GumbelBest best)
+__device__ __noinline__ GumbelBest gumbel_exact_flagged(float4 xa, float4 xb, uint4 wa, uint4 wb, uint32_t v0,
+                                                        float c, float invT, float nb, float K, GumbelBest best)
 {
     const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
     const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    uint32_t flags = 0;
 #pragma unroll
     for (int j = 0; j < N; ++j) {
         const float e = ex2(fmaf(x[j], c, nb));
-        if (__float_as_uint(fmaf(e, K, u_prime(w[j]))) & kCandBit) {
-            const float est = gumbel_score_estimate(x[j], w[j], invT);
-            const float ref = fmaxf(best.score, floor_score);
-            if (!(est < ref - estimate_margin(ref))) {
-                const float score = gumbel_score(x[j], w[j], invT);
-                const int idx = (int)(v0 + (uint32_t)j);
-                if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
+        flags |= ((__float_as_uint(fmaf(e, K, u_prime(w[j]))) >> 30) & 1u) << j;
+    }
+#pragma unroll 1
+    while (flags != 0u) {
+        const int j = __ffs(flags) - 1;
+        flags &= flags - 1u;
+        float xj = x[0];
+        uint32_t wj = w[0];
+#pragma unroll
+        for (int k = 1; k < N; ++k)
+            if (j == k) {
+                xj = x[k];
+                wj = w[k];
             }
-        }
+        const float score = gumbel_score(xj, wj, invT);
+        const int idx = (int)(v0 + (uint32_t)j);
+        if (better(score, idx, best.score, best.idx)) best = GumbelBest{score, idx};
     }
     return best;
 }
@@ -922,9 +917,9 @@ __device__ __forceinline__ void consume_batch(const uint4 (&r)[U], uint32_t jv0,
                         const uint4 wb = G8 == 8 ? make_uint4(w[o + (G8 > 4 ? 4 : 0)], w[o + (G8 > 5 ? 5 : 0)],
                                                               w[o + (G8 > 6 ? 6 : 0)], w[o + (G8 > 7 ? 7 : 0)])
                                                  : make_uint4(0u, 0u, 0u, 0u);
-                        const GumbelBest g = gumbel_exact_filtered<G8>(
+                        const GumbelBest g = gumbel_exact_flagged<G8>(
                             xa, xb, wa, wb, (jv0 + 32u * (uint32_t)u) * (uint32_t)VEC + (uint32_t)(G8 * h), rc.c, rc.invT,
-                            nb, K, bt, GumbelBest{st.best, st.bi});
+                            nb, K, GumbelBest{st.best, st.bi});
                         st.best = g.score;
                         st.bi = g.idx;
                     }

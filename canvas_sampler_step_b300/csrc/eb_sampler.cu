@@ -276,6 +276,15 @@ __device__ __forceinline__ void cp_async16_at(uint32_t dst, const uint4 *src, ui
                  : "memory");
 }
 
+// The same copy of src_size (16 or 0) bytes: the rest of the 16-byte slot is zero-filled, and
+// with 0 nothing is read.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const uint4 *src, uint32_t src_size, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+                 "r"(src_size), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 r;
@@ -284,16 +293,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return r;
 }
 
-// The nfull whole batches of a segment starting at vector j0.  The thread's staging slot for
-// ring position d and vector u is at sbase + d kDepthStride + u kSlotStride; the ring offset
-// and the global pointer advance by constants, so that no slot or address is recomputed from
-// the batch index.  One copy of the batch body, so that the masked and unmasked loops of the
-// SM's warps stay in the instruction cache together.
+// The nfull whole batches of a segment [j0, j1) starting at vector j0, and the staging of its
+// ragged last batch (vectors jf = j0 + nfull kBatch .. j1, when jf < j1) behind them: its
+// vectors at or past j1 are zero-filled without a read.  The ragged batch is left in the ring
+// for the caller, at the returned ring offset, all copies complete.  The thread's staging slot
+// for ring position d and vector u is at sbase + d kDepthStride + u kSlotStride; the ring
+// offset and the global pointer advance by constants, so that no slot or address is
+// recomputed from the batch index.  One copy of the batch body, so that the masked and
+// unmasked loops of the SM's warps stay in the instruction cache together.
 template <int VEC, int U, bool MASKED>
-__device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t nfull,
-                                              const RowCtx &rc, const PhiloxRow &ph, f32x2 c2, RowState &st,
-                                              PackedSums &q, float &nb, f32x2 &nb2, float &K, float &bt,
-                                              uint32_t sbase)
+__device__ __forceinline__ uint32_t async_batches(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
+                                                  uint32_t nfull, const RowCtx &rc, const PhiloxRow &ph, f32x2 c2,
+                                                  RowState &st, PackedSums &q, float &nb, f32x2 &nb2, float &K,
+                                                  float &bt, uint32_t sbase)
 {
     constexpr uint32_t kBatch = 32u * U;
     constexpr uint32_t kSlotStride = kDirectThreads * 16u;
@@ -303,29 +315,34 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
     const uint4 *g = src + j0 + lane;
-#pragma unroll
-    for (int k = 0; k < kAsyncDepth - 1; ++k) {
-        if ((uint32_t)k < nfull)
+    // batch k of the segment into ring offset offk: whole batches plain, the ragged one
+    // predicated vector by vector
+    auto stage_batch = [&](uint32_t k, uint32_t offk) {
+        if (k < nfull) {
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                cp_async16_at(sbase + (uint32_t)k * kDepthStride + (uint32_t)u * kSlotStride, g + k * kBatch + 32 * u,
-                              pol);
+                cp_async16_at(sbase + offk + (uint32_t)u * kSlotStride, g + k * kBatch + 32u * (uint32_t)u, pol);
+        } else if (j0 + k * kBatch < j1) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool in = j0 + k * kBatch + 32u * (uint32_t)u + lane < j1;
+                cp_async16_zfill(sbase + offk + (uint32_t)u * kSlotStride, in ? g + k * kBatch + 32u * (uint32_t)u : src + j0,
+                                 in ? 16u : 0u, pol);
+            }
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kAsyncDepth - 1; ++k) {
+        stage_batch((uint32_t)k, (uint32_t)k * kDepthStride);
         cp_async_commit();
     }
-    const uint4 *gn = g + (kAsyncDepth - 1) * kBatch;        // next batch to prefetch
     uint32_t off = 0;                                        // ring offset of the batch consumed next
     uint32_t jv = j0 + lane;
-    // batches b < nfull - (depth - 1) still prefetch batch b + depth - 1
-    const uint32_t npre = nfull > (uint32_t)(kAsyncDepth - 1) ? nfull - (uint32_t)(kAsyncDepth - 1) : 0u;
 #pragma unroll 1
     for (uint32_t b = 0; b < nfull; ++b) {
-        if (b < npre) {
-            const uint32_t offn = (off + (uint32_t)(kAsyncDepth - 1) * kDepthStride) & (kRing - 1);
-#pragma unroll
-            for (int u = 0; u < U; ++u) cp_async16_at(sbase + offn + (uint32_t)u * kSlotStride, gn + 32 * u, pol);
-        }
+        // batch b + depth - 1, whole, ragged or past the end (nothing)
+        stage_batch(b + (uint32_t)(kAsyncDepth - 1), (off + (uint32_t)(kAsyncDepth - 1) * kDepthStride) & (kRing - 1));
         cp_async_commit();
-        gn += kBatch;
         cp_async_wait<kAsyncDepth - 1>();
         uint4 r[U];
 #pragma unroll
@@ -335,19 +352,22 @@ __device__ __forceinline__ void async_batches(const K1Args &a, const uint4 *src,
         jv += kBatch;
     }
     cp_async_wait<0>();
+    return off;
 }
 
 // One row segment [j0, j1) of a warp with a deep prefetch: each lane copies the vectors it
 // will consume with cp.async (16 bytes each, L2 evict-first, no L1) into its own
 // shared-memory slots, kAsyncDepth batches ahead, and waits only for its own oldest group (no
-// cross-lane barrier).  Whole batches run in a masked or an unmasked instance of the loop; the
-// ragged remainder takes plain guarded loads.
+// cross-lane barrier).  Whole batches run in a masked or an unmasked instance of the loop.
+// The ragged last batch is staged in the ring behind them and taken vector by vector (for
+// e4m3, whose half vectors must stay in lane order, with plain guarded loads instead).
 template <int VEC, int U>
 __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src, uint32_t j0, uint32_t j1,
                                               const RowCtx &rc, f32x2 c2, RowState &st, PackedSums &q,
                                               bool gumbel, uint4 *stage)
 {
     constexpr uint32_t kBatch = 32u * U;
+    constexpr uint32_t kSlotStride = kDirectThreads * 16u;
     const uint32_t lane = threadIdx.x & 31;
     float nb = -st.xm * rc.c;
     f32x2 nb2 = pk2(nb, nb);
@@ -355,13 +375,16 @@ __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src,
     const uint32_t nfull = (j1 - j0) / kBatch;
     const uint32_t jf = j0 + nfull * kBatch;
     const uint32_t sbase = smem_addr(stage) + threadIdx.x * 16u;
+    const uint32_t js = VEC == 16 ? jf : j1;       // end of what goes through the ring
     float bt = -INFINITY;                  // the seed threshold (a lower bound of the best score)
-    if (nfull > 0) {
+    uint32_t off = 0;
+    if (j0 < js) {
         if (gumbel) {
             const PhiloxRow ph = philox_row(rc.p, rc.step, rc.sw, a.keys);
-            async_batches<VEC, U, true>(a, src, j0, nfull, rc, ph, c2, st, q, nb, nb2, K, bt, sbase);
+            off = async_batches<VEC, U, true>(a, src, j0, js, nfull, rc, ph, c2, st, q, nb, nb2, K, bt, sbase);
         } else {
-            async_batches<VEC, U, false>(a, src, j0, nfull, rc, PhiloxRow{}, c2, st, q, nb, nb2, K, bt, sbase);
+            off = async_batches<VEC, U, false>(a, src, j0, js, nfull, rc, PhiloxRow{}, c2, st, q, nb, nb2, K, bt,
+                                               sbase);
         }
     }
     if constexpr (VEC == 16) {
@@ -379,11 +402,13 @@ __device__ __forceinline__ void async_segment(const K1Args &a, const uint4 *src,
             consume_vals<8, true, true>(x, valid, h * 8u, a, rc, c2, st, q, nb, nb2, K, gumbel);
         }
     } else {
+        // the ragged batch from the ring: its vector u of every lane, u = 0, 1, .. while any
+        // lane's vector is inside the segment
 #pragma unroll 1
-        for (uint32_t jb = jf; jb < j1; jb += 32u) {
-            const uint32_t idx = jb + lane;
+        for (uint32_t u = 0; jf + 32u * u < j1; ++u) {
+            const uint32_t idx = jf + 32u * u + lane;
             const bool valid = idx < j1;
-            const uint4 r = valid ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 r = valid ? lds128(sbase + off + u * kSlotStride) : make_uint4(0u, 0u, 0u, 0u);
             consume_packed<VEC, true>(r, valid, idx, a, rc, c2, st, q, nb, nb2, K, gumbel);
         }
     }
@@ -495,6 +520,10 @@ __device__ __forceinline__ unsigned long long k2_row_start(const K2Args &a, long
 
 constexpr int kSelGeneral = 4;  // selection flag: more than 32 low-entropy candidates (bits 0-1: halt)
 constexpr int kMergeBatch = 6;   // partial states fetched per round by the selection kernel
+// The selection kernel stages a canvas's partial states (one contiguous slot range on the
+// streaming partition) in shared memory when the range holds at most this many slots.
+constexpr int kK2StageSlots = 4096;
+constexpr int kK2StageBytes = kK2StageSlots * (int)sizeof(Partial);
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 {
@@ -528,10 +557,11 @@ __device__ __forceinline__ unsigned long long entropy_key(float H, int p)
 // nothing, only when W < G).
 // `half` (0 or 1): this thread merges the first or the second half of the row's slots (the two
 // threads of a row combine their halves in that order afterwards).
+// `staged` (streaming partition only): the slots from staged_first on, copied to shared memory.
 __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *partials, const int2 *rowunits,
                                              unsigned long long W, unsigned long long G, long long r, float c,
                                              int half, RowState &st, int &flags, const int2 *local_units = nullptr,
-                                             int p = 0)
+                                             int p = 0, const Partial *staged = nullptr, long long staged_first = 0)
 {
     long long base, stride;
     int n;
@@ -548,6 +578,20 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
     }
     const int h = (n + 1) >> 1;
     const int lo = half ? h : 0, hi = half ? n : h;
+    if (staged) {
+        // from shared memory: a plain loop in slot order
+#pragma unroll 1
+        for (int i = lo; i < hi; ++i) {
+            if (W < G) {
+                const unsigned long long cu = (unsigned long long)(base - r + i);
+                if (cu * W / G >= (cu + 1) * W / G) continue;
+            }
+            const Partial q = staged[base + i - staged_first];
+            merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, c);
+            flags |= q.flags;
+        }
+        return;
+    }
     // loads in batches of kMergeBatch independent requests, merged in slot order
     for (int i0 = lo; i0 < hi; i0 += kMergeBatch) {
         Partial q[kMergeBatch];
@@ -604,6 +648,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
     __shared__ int n_gather, n_acc, sel_status, sel_committed, sel_flag, sel_stop, sel_ns, sel_nm, sel_cap;
     __shared__ float sel_mean;
     __shared__ unsigned long long sel_bigmin;
+    extern __shared__ __align__(16) unsigned char k2_stage[];   // kK2StageBytes: staged partials
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -658,6 +703,30 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         Wloc = Wt;
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // On the streaming partition the canvas's partial states are one contiguous slot range, from
+    // its first row's first unit to its last row's last unit: every thread copies its share of
+    // it to shared memory at once (one round trip), and the rows merge from there.
+    const Partial *staged = nullptr;
+    long long staged_first = 0;
+    if (a.k3_g == 0) {
+        if (local) __syncthreads();               // Ru complete
+        const int2 uf = local ? Ru[0] : a.rowunits[rowbase];
+        const int2 ul = local ? Ru[L - 1] : a.rowunits[rowbase + L - 1];
+        const long long s0 = rowbase + uf.x, s1 = rowbase + L - 1 + ul.y;
+        if (s1 >= s0 && s1 - s0 < (long long)kK2StageSlots) {
+            Partial *pst = reinterpret_cast<Partial *>(k2_stage);
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.partials + s0);
+            const uint32_t dst = smem_addr(pst);
+            const int nchunk = (int)(s1 - s0 + 1) * (int)(sizeof(Partial) / 16);
+            for (int i = tid; i < nchunk; i += blockDim.x)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (uint32_t)i), "l"(src + i)
+                             : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            staged = pst;
+            staged_first = s0;
+        }
+    }
     const unsigned long long W = local ? Wloc : k2_row_start(a, a.rows);
     const unsigned long long G = (unsigned long long)a.G;
     const unsigned long long Wr = !a.raw_partials ? 0ull
@@ -678,7 +747,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const long long r = rowbase + (row_here ? p : 0);
         RowState st = empty_state();
         int flags = 0;
-        if (row_here) k2_merge_row(a, a.partials, a.rowunits, W, G, r, cb, half, st, flags, local ? Ru : nullptr, p);
+        if (row_here)
+            k2_merge_row(a, a.partials, a.rowunits, W, G, r, cb, half, st, flags, local ? Ru : nullptr, p, staged,
+                         staged_first);
         pair_combine(st, flags, cb);
         RowState sr = empty_state();
         int rflags = 0;
@@ -1028,7 +1099,9 @@ eb_status geometry(int *grid_out, int kind)
              cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kBF16Vec, ebk::kDirectU>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess ||
              cudaFuncSetAttribute(ebk::k1_rowstats_direct<ebk::kFP8Vec, ebk::kFP8U>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess))
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kDirectStageBytes) != cudaSuccess ||
+             cudaFuncSetAttribute(ebk::k2_select, cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kK2StageBytes) !=
+                 cudaSuccess))
             return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
         (void)smem_optin;
         // one CTA of kDirectWarps warps per SM; every warp is one unit of the row partition
@@ -1071,7 +1144,9 @@ eb_status unembed_geometry(int *nsm_out)
         if (cudaFuncSetAttribute(ebk::k3::k3_unembed<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess ||
             cudaFuncSetAttribute(ebk::k3::k3_unembed<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+                                 (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(ebk::k2_select, cudaFuncAttributeMaxDynamicSharedMemorySize, ebk::kK2StageBytes) !=
+                cudaSuccess)
             return fail(EB_ERR_CUDA, "cudaFuncSetAttribute failed");
         g.nsm = nsm;
         g.ready.store(1, std::memory_order_release);
@@ -1274,7 +1349,7 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(ebk::kK2Threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = ebk::kK2StageBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -80,13 +80,14 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--logits", choices=("bf16", "fp8"), default="bf16",
                     help="element type of the single-step workload's logits (fp8: OCP e4m3)")
-    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "loop1", "blocks"),
+    ap.add_argument("--workload", choices=("single", "fused", "fused1", "loop", "loop1", "stop", "blocks"),
                     default="single",
                     help="single: the single-step workload (default, the headline line); fused: "
                          "the fused unembedding + sampler step (4 x 256 positions, K=2048); "
                          "fused1: the same for one canvas (256 positions); loop: the adaptive "
                          "48-step loop over 8 canvases with the stand-in denoiser; loop1: the "
-                         "same for one canvas; blocks: the block driver, 64 blocks on 8 slots")
+                         "same for one canvas; stop: a one-canvas loop that the adaptive stop "
+                         "ends early; blocks: the block driver, 64 blocks on 8 slots")
     ap.add_argument("--no-extras", action="store_true",
                     help="headline only: leave out the per-workload records")
     return ap.parse_args(argv)
@@ -973,6 +974,8 @@ def extras(args, device, local):
                                   device, local)
     out["loop_b8"] = measure_loop(eb_synth.cfg3(), "mixed batch of eight, peak growth 0.1-0.8", 3, 1,
                                   device, local)
+    out["loop_stop"] = measure_loop(eb_synth.cfg_stop(), "early stop, one canvas, sigma 1, peak growth 0.5", 5,
+                                    1, device, local)
     torch.cuda.empty_cache()
     fp8 = argparse.Namespace(**{**vars(args), "logits": "fp8", "steps": 200, "warmup": 5})
     lk = logits_kind(fp8, eb, torch)
@@ -1012,10 +1015,11 @@ def run_workload(args, rank, world, local):
     if args.workload in ("fused", "fused1"):
         FB = 1 if args.workload == "fused1" else 4
         out = measure_fused(FB, args.steps, args.warmup, args.e2e_steps, device, local, dist, world)
-    elif args.workload in ("loop", "loop1"):
-        cfg = eb_synth.cfg3() if args.workload == "loop" else eb_synth.cfg2()
-        label = ("mixed batch of eight, peak growth 0.1-0.8" if args.workload == "loop"
-                 else "full adaptive loop, one canvas, peak growth 0.3")
+    elif args.workload in ("loop", "loop1", "stop"):
+        cfg = {"loop": eb_synth.cfg3, "loop1": eb_synth.cfg2, "stop": eb_synth.cfg_stop}[args.workload]()
+        label = {"loop": "mixed batch of eight, peak growth 0.1-0.8",
+                 "loop1": "full adaptive loop, one canvas, peak growth 0.3",
+                 "stop": "early stop, one canvas, sigma 1, peak growth 0.5"}[args.workload]
         out = measure_loop(cfg, label, max(1, args.steps // 200), max(1, args.warmup // 100), device, local,
                            dist, world)
     else:

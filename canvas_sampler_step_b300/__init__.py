@@ -12,7 +12,12 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .build import LIB_PATH, build  # noqa: F401
+from .build import CHECKS_LIB_PATH, build, build_checks  # noqa: F401
+from .build import LIB_PATH as _DEFAULT_LIB_PATH
+
+# The library this process loads: libeb_sampler.so, or another build of the same sources named
+# by EB_SAMPLER_LIB (for instance the checked build, CHECKS_LIB_PATH).
+LIB_PATH = os.environ.get("EB_SAMPLER_LIB") or _DEFAULT_LIB_PATH
 
 EB_OK, EB_ERR_INVALID, EB_ERR_CUDA, EB_ERR_UNSUPPORTED, EB_ERR_WORKSPACE, EB_ERR_CALLBACK = range(6)
 EB_F32, EB_BF16, EB_FP8_E4M3 = 0, 1, 2
@@ -20,6 +25,7 @@ EB_RUNNING, EB_STOP_ADAPTIVE, EB_STOP_COMPLETE, EB_STOP_CAP = 0, 1, 2, 3
 EB_STATUS_NONFINITE = 0x100
 EB_STATUS_TIMEOUT = 0x200
 EB_SLOT_IDLE = 0x400
+EB_STATUS_CHECK = 0x800
 EB_FLAG_DIAG_STALL = 1
 EB_FLAG_STOP_MASKED_ONLY = 2
 EB_FLAG_FINALIZE_SAMPLED = 4
@@ -28,7 +34,8 @@ EB_FLAG_STOP_RAW_ENTROPY = 8
 EXPORTED = ("eb_default_params", "eb_temperature", "eb_workspace_bytes", "eb_sampler_step",
             "eb_sample_canvas", "eb_status_string", "eb_last_error", "eb_set_profile_events",
             "eb_unembed_workspace_bytes", "eb_unembed_sample", "eb_unembed_logits",
-            "eb_sampler_step_noalloc", "eb_blocks_workspace_bytes", "eb_sample_blocks")
+            "eb_sampler_step_noalloc", "eb_blocks_workspace_bytes", "eb_sample_blocks",
+            "eb_checks_enabled", "eb_check_word")
 
 
 class EbParams(ctypes.Structure):
@@ -78,6 +85,10 @@ def lib() -> ctypes.CDLL:
     L.eb_status_string.restype = ctypes.c_char_p
     L.eb_last_error.argtypes = []
     L.eb_last_error.restype = ctypes.c_char_p
+    L.eb_checks_enabled.argtypes = []
+    L.eb_checks_enabled.restype = i32
+    L.eb_check_word.argtypes = [i32]
+    L.eb_check_word.restype = ctypes.c_uint32
     L.eb_set_profile_events.argtypes = [P, P]
     L.eb_set_profile_events.restype = i32
     L.eb_unembed_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -119,6 +130,16 @@ def _stream(stream):
 def _check(status: int):
     if status != EB_OK:
         raise EbError(status, lib().eb_last_error().decode() or lib().eb_status_string(status).decode())
+
+
+def eb_checks_enabled() -> bool:
+    """True for the checked debug build (device bounds checks, EB_STATUS_CHECK)."""
+    return bool(lib().eb_checks_enabled())
+
+
+def eb_check_word(clear: bool = False) -> int:
+    """The checked build's device word of failed bounds checks (0 in the normal build)."""
+    return int(lib().eb_check_word(1 if clear else 0))
 
 
 def eb_default_params(seed: int = 0, **overrides) -> EbParams:

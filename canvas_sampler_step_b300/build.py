@@ -36,9 +36,19 @@ def nvcc_shared(src: str, out: str, include_dir: str, deps, extra=(), force: boo
     return out
 
 
+CHECKS_LIB_PATH = os.path.join(PKG, "libeb_sampler_checks.so")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     return nvcc_shared(SRC, LIB_PATH, os.path.join(ROOT, "include"), [HDR], force=force,
                        verbose=verbose)
+
+
+def build_checks(force: bool = False, verbose: bool = False) -> str:
+    """The checked debug build (-DEB_CHECKS): device bounds checks that record a status bit
+    instead of trapping (eb_check_word in the header)."""
+    return nvcc_shared(SRC, CHECKS_LIB_PATH, os.path.join(ROOT, "include"), [HDR], extra=["-DEB_CHECKS"],
+                       force=force, verbose=verbose)
 
 
 if __name__ == "__main__":

@@ -93,6 +93,26 @@ struct RowState {
     int bi;
 };
 
+// Bounds checks of the debug build (compiled with -DEB_CHECKS): a failed check records a bit
+// in a device word and the access it guards is skipped; nothing traps.  The selection kernel
+// then or-s EB_STATUS_CHECK into the status of the canvases it decides.  In the normal build
+// EB_CHECK(c) is the constant true and costs nothing.
+#ifdef EB_CHECKS
+__device__ unsigned int g_check_word;
+__device__ __forceinline__ bool eb_check_ok(bool ok, unsigned int bit)
+{
+    if (!ok) atomicOr(&g_check_word, bit);
+    return ok;
+}
+#define EB_CHECK(cond, bit) ::ebk::eb_check_ok((cond), (bit))
+#else
+#define EB_CHECK(cond, bit) true
+#endif
+constexpr unsigned int kCheckPartialSlot = 1u;   // a partial-state slot outside the workspace
+constexpr unsigned int kCheckRow = 2u;           // a row or position index outside its array
+constexpr unsigned int kCheckSegment = 4u;       // a row segment outside its row
+constexpr unsigned int kCheckUnits = 8u;         // a row's partition units out of order or range
+
 struct K1Args {
     const void *logits;
     const uint8_t *mask;
@@ -117,6 +137,9 @@ struct K1Args {
     const float *canvas_c;
     const float *canvas_invT;
     int raw;                // 1: every row as unmasked (no sampling), for the raw-logit entropy
+#ifdef EB_CHECKS
+    long long nslots;       // partial-state slots in the workspace (bounds checks)
+#endif
 };
 
 struct K2Args {
@@ -161,6 +184,9 @@ struct K2Args {
                                // row block mb, group rank j < k3_g and column group hh <
                                // k3_groups write slot ((mb k3_g + j) k3_groups + hh) 128 + row % 128
     int k3_groups;
+#ifdef EB_CHECKS
+    long long nslots;          // partial-state slots in the workspace (bounds checks)
+#endif
 };
 
 // ---------------------------------------------------------------- small device helpers

@@ -215,7 +215,8 @@ __device__ __forceinline__ void reduce_and_store(RowState st, const K1Args &a, f
         RowState s2 = lane < kConsumerWarps ? red[lane] : empty_state();
         const uint32_t nf = __reduce_or_sync(0xFFFFFFFFu, lane < kConsumerWarps ? redflag[lane] : 0u);
         warp_merge(s2, c);
-        if (lane == 0) write_partial(&a.partials[row + blockIdx.x], s2, flags | (int)nf);
+        if (lane == 0 && EB_CHECK((long long)row + blockIdx.x < a.nslots, kCheckPartialSlot))
+            write_partial(&a.partials[row + blockIdx.x], s2, flags | (int)nf);
     }
     consumer_sync();
 }
@@ -439,6 +440,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
     int row;
     long long j0, j1;
     while (cur.next(row, j0, j1)) {
+        if (!EB_CHECK(row >= 0 && row < a.rows && j0 >= 0 && j0 <= j1 && j1 <= a.nvec_row, kCheckSegment)) continue;
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
         const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) k1_rowstats_direct(const K1
         packed_fold(q, st);
         const bool nan_here = __any_sync(0xFFFFFFFFu, isnan(st.S) || isnan(st.T2));
         warp_merge(st, rc.c);
-        if (lane == 0) {
+        if (lane == 0 && EB_CHECK((long long)row + gw < a.nslots, kCheckPartialSlot)) {
             write_partial(&a.partials[row + gw], st, nan_here ? kPartialNonfinite : 0);
             if (cur.first) a.rowunits[row].x = gw;
             if (cur.last) a.rowunits[row].y = gw;
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(kConsumers, 1) k1_rowstats_scalar(const K1Args
     int row;
     long long j0, j1;
     while (cur.next(row, j0, j1)) {
+        if (!EB_CHECK(row >= 0 && row < a.rows && j0 >= 0 && j0 <= j1 && j1 <= a.nvec_row, kCheckSegment)) continue;
         const int b = row / a.L;
         if (!a.weighted && a.status[b] != EB_RUNNING) continue;
         const RowCtx rc = row_ctx(a, b, (uint32_t)(row - b * a.L));
@@ -575,6 +578,7 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
         base = r + u.x;
         stride = 1;
         n = u.y - u.x + 1;
+        if (!EB_CHECK(u.x >= 0 && u.x <= u.y && (unsigned long long)u.y < G, kCheckUnits)) n = 0;
     }
     const int h = (n + 1) >> 1;
     const int lo = half ? h : 0, hi = half ? n : h;
@@ -586,6 +590,8 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
                 const unsigned long long cu = (unsigned long long)(base - r + i);
                 if (cu * W / G >= (cu + 1) * W / G) continue;
             }
+            if (!EB_CHECK(base + i >= staged_first && base + i - staged_first < (long long)kK2StageSlots, kCheckPartialSlot))
+                continue;
             const Partial q = staged[base + i - staged_first];
             merge_state(st, q.xm, q.S, q.T2, q.ai, q.best, q.bi, c);
             flags |= q.flags;
@@ -597,7 +603,11 @@ __device__ __forceinline__ void k2_merge_row(const K2Args &a, const Partial *par
         Partial q[kMergeBatch];
 #pragma unroll
         for (int k = 0; k < kMergeBatch; ++k)
-            if (i0 + k < hi) q[k] = partials[base + (long long)(i0 + k) * stride];
+            if (i0 + k < hi) {
+                const long long slot = base + (long long)(i0 + k) * stride;
+                if (EB_CHECK(slot >= 0 && slot < a.nslots, kCheckPartialSlot)) q[k] = partials[slot];
+                else q[k] = Partial{-INFINITY, 0.0f, 0.0f, 0x7FFFFFFF, -INFINITY, -1, 0, 0};
+            }
 #pragma unroll
         for (int k = 0; k < kMergeBatch; ++k) {
             if (i0 + k >= hi) break;
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         const int2 uf = local ? Ru[0] : a.rowunits[rowbase];
         const int2 ul = local ? Ru[L - 1] : a.rowunits[rowbase + L - 1];
         const long long s0 = rowbase + uf.x, s1 = rowbase + L - 1 + ul.y;
-        if (s1 >= s0 && s1 - s0 < (long long)kK2StageSlots) {
+        if (s1 >= s0 && s1 - s0 < (long long)kK2StageSlots && EB_CHECK(s0 >= 0 && s1 < a.nslots, kCheckPartialSlot)) {
             Partial *pst = reinterpret_cast<Partial *>(k2_stage);
             const uint4 *src = reinterpret_cast<const uint4 *>(a.partials + s0);
             const uint32_t dst = smem_addr(pst);
@@ -876,7 +886,8 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
                 }
             }
             const int pos = (int)(k & 0xFFFFFFFFu);
-            const unsigned long long h = lane < ns ? Hq[pos] : 0ull;
+            const bool pos_ok = lane < ns && EB_CHECK(pos >= 0 && pos < L, kCheckRow);
+            const unsigned long long h = pos_ok ? Hq[pos] : 0ull;
             unsigned long long incl = h;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -885,7 +896,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
             }
             const unsigned long long excl = incl - h;
             const bool acc = lane < ns && (lane == 0 || (long long)excl <= a.bound_q);
-            if (acc) Acc[pos] = 1;
+            if (acc && pos_ok) Acc[pos] = 1;
             const unsigned acc_mask = __ballot_sync(0xFFFFFFFFu, acc);
             const unsigned ok_mask = __ballot_sync(0xFFFFFFFFu, acc || lane >= ns);
             const unsigned long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
@@ -893,7 +904,8 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
                 int nacc = __popc(acc_mask);
                 // sorted index ns: the lowest-entropy position above the bound
                 if (bigmin != ~0ull && (ns == 0 || (ok_mask == 0xFFFFFFFFu && (long long)tot <= a.bound_q))) {
-                    Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
+                    const int bp = (int)(bigmin & 0xFFFFFFFFu);
+                    if (EB_CHECK(bp >= 0 && bp < L, kCheckRow)) Acc[bp] = 1;
                     ++nacc;
                 }
                 const int left = nm - nacc;
@@ -915,6 +927,9 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         // non-finite logits or a wait that gave up: the canvas halts with nothing committed
         if (tid == 0) {
             a.status[b] = ((flag & 1) ? EB_STATUS_NONFINITE : 0) | ((flag & 2) ? EB_STATUS_TIMEOUT : 0);
+#ifdef EB_CHECKS
+            if (g_check_word) a.status[b] |= EB_STATUS_CHECK;
+#endif
             if (a.steps_taken) a.steps_taken[b] = step + 1;
             if (a.committed) a.committed[b] = 0;
             if (a.mean_entropy) a.mean_entropy[b] = NAN;
@@ -931,7 +946,7 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         for (int p = tid; p < L; p += blockDim.x) {
             if (Ms[p] && (long long)Hq[p] <= a.bound_q) {
                 const int i = atomicAdd(&n_gather, 1);
-                keys[i] = entropy_key(Hf[p], p);
+                if (EB_CHECK(i < kMaxL, kCheckRow)) keys[i] = entropy_key(Hf[p], p);
             }
         }
         int n2 = 1;
@@ -955,8 +970,10 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
             }
         }
         // inclusive scan of the sorted fixed-point entropies (Hillis-Steele)
-        for (int i = tid; i < n2; i += blockDim.x)
-            scanbuf[i] = i < ns ? Hq[(int)(keys[i] & 0xFFFFFFFFu)] : 0ull;
+        for (int i = tid; i < n2; i += blockDim.x) {
+            const int pk = i < ns ? (int)(keys[i] & 0xFFFFFFFFu) : -1;
+            scanbuf[i] = i < ns && EB_CHECK(pk >= 0 && pk < L, kCheckRow) ? Hq[pk] : 0ull;
+        }
         __syncthreads();
         for (int off = 1; off < n2; off <<= 1) {
             unsigned long long add[kMaxL / kK2Threads];
@@ -971,7 +988,8 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         for (int i = tid; i < ns; i += blockDim.x) {
             const unsigned long long excl = i == 0 ? 0ull : scanbuf[i - 1];
             if (i == 0 || (long long)excl <= a.bound_q) {
-                Acc[(int)(keys[i] & 0xFFFFFFFFu)] = 1;
+                const int pk = (int)(keys[i] & 0xFFFFFFFFu);
+                if (EB_CHECK(pk >= 0 && pk < L, kCheckRow)) Acc[pk] = 1;
                 ++my_acc;
             } else {
                 my_rej = 1;
@@ -982,7 +1000,8 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         if (tid == 0) {
             int nacc = n_acc;
             if (bigmin != ~0ull && all_acc && (long long)scanbuf[ns - 1] <= a.bound_q) {
-                Acc[(int)(bigmin & 0xFFFFFFFFu)] = 1;
+                const int bp = (int)(bigmin & 0xFFFFFFFFu);
+                if (EB_CHECK(bp >= 0 && bp < L, kCheckRow)) Acc[bp] = 1;
                 ++nacc;
             }
             const int left = nm - nacc;
@@ -1020,6 +1039,10 @@ __global__ void __launch_bounds__(kK2Threads) k2_select(const K2Args a)
         if (a.mean_entropy) a.mean_entropy[b] = mean;
         if (a.committed_hist) a.committed_hist[(long long)b * a.max_steps + step] = committed;
         if (a.mean_hist) a.mean_hist[(long long)b * a.max_steps + step] = mean;
+#ifdef EB_CHECKS
+        __threadfence();
+        if (g_check_word) a.status[b] |= EB_STATUS_CHECK;
+#endif
     }
 }
 
@@ -1305,6 +1328,12 @@ eb_status launch_select(const eb_params *params, int B, int L, int step, float c
                         const RawPass &raw = RawPass())
 {
     ebk::K2Args a2;
+#ifdef EB_CHECKS
+    // partial-state slots: the streaming layout, or the fused kernel's (row block, group rank,
+    // column group, row) layout
+    a2.nslots = k3_g > 0 ? (long long)((rows + ebk::k3::BM - 1) / ebk::k3::BM) * k3_g * ebk::k3::kEpiGroups * ebk::k3::BM
+                         : (long long)rows + ebk::kMaxGrid;
+#endif
     a2.partials = partials;
     a2.prefix = prefix;
     a2.rowunits = rowunits;
@@ -1437,6 +1466,9 @@ eb_status launch_step(const eb_params *params, int B, int L, int V, eb_dtype dty
     a1.canvas_c = sb.canvas_c;
     a1.canvas_invT = sb.canvas_invT;
     a1.raw = 0;
+#ifdef EB_CHECKS
+    a1.nslots = rows + ebk::kMaxGrid;
+#endif
     // EB_FLAG_STOP_RAW_ENTROPY: first a pass at T = 1 with every row unmasked (no sampling)
     // into the second workspace copy; the selection kernel sums its entropies for the stop rule
     RawPass raw;
@@ -2035,6 +2067,31 @@ eb_status eb_set_profile_events(void *k1_begin, void *k1_end)
     g_profile_begin = static_cast<cudaEvent_t>(k1_begin);
     g_profile_end = static_cast<cudaEvent_t>(k1_end);
     return ok();
+}
+
+int eb_checks_enabled(void)
+{
+#ifdef EB_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+uint32_t eb_check_word(int clear)
+{
+#ifdef EB_CHECKS
+    unsigned int w = 0;
+    if (cudaMemcpyFromSymbol(&w, ebk::g_check_word, sizeof w) != cudaSuccess) return 0;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(ebk::g_check_word, &z, sizeof z) != cudaSuccess) return 0;
+    }
+    return w;
+#else
+    (void)clear;
+    return 0;
+#endif
 }
 
 }  // extern "C"

@@ -316,6 +316,13 @@ def cfg2(seed: int = 0, L: int = 256, V: int = 262144) -> Peaked:
     return Peaked(1, L, V, "bf16", 3.0, 0.0, 4.0, (0.3,), (seed,))
 
 
+def cfg_stop(seed: int = 7, L: int = 256, V: int = 262144) -> Peaked:
+    """The early-stop loop: one canvas whose peaks (sigma 1, U(12, 14) + 0.5 s) soon dominate,
+    so that the mean entropy falls below the stop threshold while positions are still masked
+    and the adaptive stop ends the loop (after 9 of at most 48 steps for seed 7)."""
+    return Peaked(1, L, V, "bf16", 1.0, 12.0, 2.0, (0.5,), (seed,))
+
+
 CFG3_RATES = (0.1, 0.2, 0.4, 0.8)
 
 

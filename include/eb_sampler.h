@@ -70,6 +70,8 @@ typedef enum { EB_F32 = 0, EB_BF16 = 1, EB_FP8_E4M3 = 2 } eb_dtype;
 #define EB_STATUS_NONFINITE 0x100 /* or-ed in: NaN / +-Inf logits seen; canvas halted */
 #define EB_STATUS_TIMEOUT 0x200   /* or-ed in: a bounded device wait gave up; canvas halted */
 #define EB_SLOT_IDLE 0x400        /* eb_sample_blocks: a slot holding no block */
+#define EB_STATUS_CHECK 0x800     /* or-ed in (checked build only): a device bounds check failed
+                                     (eb_check_word); canvas halted */
 
 typedef struct {
     int32_t max_steps;     /* 48 */
@@ -315,6 +317,22 @@ const char *eb_status_string(eb_status s);
 
 /* Description of the last error returned on the calling thread ("" if none). */
 const char *eb_last_error(void);
+
+/* The checked debug build.  The same sources compiled with -DEB_CHECKS (the library
+ * libeb_sampler_checks.so next to libeb_sampler.so) test, before every access whose index the
+ * streaming and selection kernels compute (partial-state slots, row segments, partition units,
+ * selected positions), that it lies inside its array.  A failed check skips the access, sets a
+ * bit in a device word of the library (1: partial-state slot, 2: row or position, 4: row
+ * segment, 8: partition units) and never traps; the selection kernel then or-s
+ * EB_STATUS_CHECK into the status of the canvases it decides, which halts them.  The word
+ * stays set until read with clear = 1.  The checks cover the streaming path; the fused
+ * kernel's own writes are not checked.
+ *
+ * eb_checks_enabled: 1 in the checked build, 0 in the normal one.
+ * eb_check_word: the device word's bits (0 in the normal build); clear != 0 resets it to 0.
+ * Synchronous (it copies the word to the host); returns 0 if the copy fails. */
+int eb_checks_enabled(void);
+uint32_t eb_check_word(int clear);
 
 #ifdef __cplusplus
 }

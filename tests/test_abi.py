@@ -42,6 +42,20 @@ def test_every_declared_symbol_is_exported(libs):
     assert set(eb.EXPORTED) <= decl
 
 
+def test_checked_build_exports_the_same_symbols(libs):
+    """The checked debug build (-DEB_CHECKS) is the same library with device bounds checks: it
+    exports every declared function, says it is the checked build, and the normal one does
+    not (neither call needs a device)."""
+    eb.build_checks()
+    checked = ctypes.CDLL(eb.CHECKS_LIB_PATH)
+    for name in _declared("eb_sampler.h"):
+        assert hasattr(checked, name), name
+    checked.eb_checks_enabled.restype = ctypes.c_int
+    assert checked.eb_checks_enabled() == 1
+    assert not eb.eb_checks_enabled() or os.environ.get("EB_SAMPLER_LIB")
+    assert eb.eb_check_word() == 0 or eb.eb_checks_enabled()
+
+
 def test_default_params_are_the_recommended_settings(libs):
     p = eb.eb_default_params()
     assert p.max_steps == 48

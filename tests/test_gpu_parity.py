@@ -372,6 +372,23 @@ def test_loop_full_size_adaptive_one_canvas():
     _loop_in_one_call(cfg, params_pair(seed=0)[0], hist[-1])
 
 
+def test_loop_full_size_adaptive_stop():
+    """The early-stop loop at full size (B=1, 256 x 262144 bf16, sigma 1, peaks U(12, 14) +
+    0.5 s): the mean entropy falls below 0.005 with positions still masked, so the adaptive stop
+    ends the loop well before the cap, and the still-masked positions take the argmax.  Every
+    step is compared with the oracle; the stop step, stop reason and tokens equal the oracle's."""
+    cfg = eb_synth.cfg_stop()
+    rep, hist, c, ost, parted = _lockstep(cfg, device_generator=True, label="early stop, B=1",
+                                          resync_ties=True)
+    _check_loop_against_oracle(cfg, rep, hist, ost, parted)
+    final = hist[-1]
+    assert final["status"][0] == eb.EB_STOP_ADAPTIVE, final["status"]
+    assert final["steps_taken"][0] < 48
+    committed = [int(h["committed"][0]) for h in hist]
+    assert committed[-1] > 1 and sum(committed) == 256     # the stop commits the rest at once
+    _loop_in_one_call(cfg, params_pair(seed=cfg.seeds[0])[0], hist[-1])
+
+
 def test_loop_full_size_batch_of_eight():
     """B=8, L=256, V=262144 bf16, rates (0.1, 0.2, 0.4, 0.8), up to 48 steps: every step of every
     running canvas compared with the oracle element by element, steps to stop per canvas equal

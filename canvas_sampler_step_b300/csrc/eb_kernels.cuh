@@ -17,7 +17,8 @@
 //     one for e4m3, whose vector holds 16 logits) with cp.async (L2 evict-first, no L1) into
 //     its own shared-memory slots four batches ahead of use, and waits only for its own
 //     oldest group; the slot offset and the global pointer advance by constants.  Whole
-//     batches run without bounds checks, the ragged tail with guarded plain loads.  (A TMA
+//     batches run without bounds checks; the ragged last batch is staged in the same ring
+//     (vectors past the segment zero-filled without a read) and taken vector by vector.  (A TMA
 //     bulk-copy ring with a producer warp measured slower on this workload, its consumers
 //     idling on the ring's barriers; register double buffering had too little in flight.)
 //   * Per element: t = x * log2(e)/T - xm * log2(e)/T, e = 2^t (MUFU), S += e, T2 += t e,
@@ -26,15 +27,18 @@
 //     A batch takes one new-maximum vote, so the rare rescale stays a branch.
 //   * Gumbel-max for masked rows: with u from a Philox4x32-10 word and E = -ln u, the sample
 //     maximises z - ln E.  Since E >= 1 - u, an entry can beat the best score so far only if
-//     1 - u < 2^t K, K = 2^(xm log2e / T - best log2e); one candidate vote per batch.  Entries
-//     that pass (a handful per warp and row) take the exact score z - logf(-log1pf(-(1 - u)))
-//     in an out-of-line function, handed the Philox words already drawn; the warp shares its
-//     best score when it moves.
+//     1 - u < 2^t K, K = 2^(xm log2e / T - best log2e); one candidate vote per batch.  A
+//     segment's first batch sets the threshold from the score estimates of all its entries
+//     (their maximum less the estimate's error).  Entries that pass later (about one per
+//     record of the best score) take the exact score z - logf(-log1pf(-(1 - u))) in an
+//     out-of-line function, handed the Philox words already drawn; the warp shares its best
+//     score when it moves.
 //   * Optional per-canvas step, temperature and Philox canvas id (the block driver), and a
 //     sampling-free raw mode at T = 1 (the raw-logit entropy of the stop rule's variant).
-// k2_select (one CTA per canvas) merges each row's partials in ascending unit order
-// (deterministic), runs the stop test, the entropy-bounded selection and the commit /
-// re-mask / finalisation.  Sums of entropies are exact 64-bit fixed point (2^-40 nats).
+// k2_select (one CTA per canvas) copies the canvas's contiguous range of partial states to
+// shared memory, merges each row's partials in ascending unit order (deterministic), runs the
+// stop test, the entropy-bounded selection and the commit / re-mask / finalisation.  Sums of
+// entropies are exact 64-bit fixed point (2^-40 nats).
 #pragma once
 
 #include <cuda_runtime.h>

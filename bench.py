@@ -613,7 +613,35 @@ def cpu_baseline():
             "one_thread_value": 1.0 / dt1,
             "sample": "full steps of seed 0 (256 rows x 262144 bf16, 128 masked), all rows and the "
                       f"selection: median of 3 on {cores} threads ({dt:.2f} s wall each), "
-                      f"1 on one thread ({dt1:.2f} s)"}
+                      f"1 on one thread ({dt1:.2f} s)",
+            "parity": step_parity(x, mask)}
+
+
+def step_parity(x, mask):
+    """The library's step next to the oracle's on the same input (seed 0 of the workload),
+    with the near-ties counted as the parity tests count them: entropy error, argmax and
+    sample mismatches, and whether the selection matched."""
+    import torch
+
+    import canvas_sampler_step_b300 as eb
+    import oracle
+    st = oracle.State.fresh(B, L, mask)
+    res = oracle.step(x, st, 0, oracle.Params(seed=0), temperature=float(np.float32(TEMPERATURE)))
+    c = eb.Canvas(B, L, V, eb.EB_BF16, mask=mask)
+    c.step(eb.eb_default_params(seed=0), torch.from_numpy(x.view(np.int16)).cuda(), 0, TEMPERATURE)
+    torch.cuda.synchronize()
+    H = c.entropy.cpu().numpy().astype(np.float64)
+    A = c.argmax.cpu().numpy()
+    Y = c.sampled.cpu().numpy()
+    masked = mask.astype(bool)
+    ydiff = masked & (Y != res.Y)
+    ties = res.gap < 1e-6
+    canvas_tie = bool((res.sum_margin <= 1e-5).any() or (res.order_margin <= 2e-5).any())
+    return {"rows": int(B * L), "max_abs_dH": float(np.abs(H - res.H).max()),
+            "argmax_mismatch": int((A != res.A).sum()),
+            "sample_mismatch": int((ydiff & ~ties).sum()), "sample_ties": int((ydiff & ties).sum()),
+            "selection_equal": bool(np.array_equal(c.mask.cpu().numpy(), st.mask)),
+            "canvas_tie": canvas_tie}
 
 
 def run_reference(args, rank, world, local):

@@ -254,16 +254,6 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2 *p)
     return r;
 }
 
-// Plain 16-byte load of the ragged tail of a segment (bypassing L1, evict-first in L2).
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p), "l"(evict_first_policy()));
-    return r;
-}
-
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait()

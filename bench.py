@@ -44,7 +44,7 @@ K1_SAMPLES = 100                         # row-statistics launches timed one by 
 WARM_SECONDS = 0.5                       # least time of warm-up steps before any timed work
 BYTES_PER_STEP = B * L * V * 2           # algorithmic bytes: every logit read once
 TEMPERATURE = 0.8
-SUBMIT_SLEEP_CYCLES = 200_000        # GPU clock cycles slept before a timed region starts
+FLUSH_ELEMS = 1 << 29                # int16 elements (1 GiB) written right before a timed region
 WORKLOAD = ("single EB sampler step: B=1 canvas, L=256 positions, V=262144 bf16 logits "
             "(2.5*N(0,1) + U(0,12) peak per position), 128 of 256 masked, T=0.8")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k1_rowstats_bf16_single_step.md")
@@ -438,10 +438,12 @@ def run_single(args, lk, device, local, dist, world, timed=True):
     end = torch.cuda.Event(enable_timing=True)
     barrier(dist, local)
     torch.cuda.synchronize()
+    flush = torch.empty(FLUSH_ELEMS, dtype=torch.int16, device=device)
     with ClockSampler(local) as clocks:
-        # a bounded GPU sleep (about 0.1 ms) ahead of the start event keeps the host's graph
-        # submission out of the device time: the replays are queued before the event runs
-        torch.cuda._sleep(SUBMIT_SLEEP_CYCLES)
+        # writing 1 GiB (far more than L2) right before the start event flushes L2 and keeps the
+        # GPU and its memory busy while the host queues the replays, so that the host's graph
+        # submission stays out of the device time
+        flush.fill_(1)
         start.record(stream)
         for r in range(R):
             if r > 0:
@@ -450,6 +452,7 @@ def run_single(args, lk, device, local, dist, world, timed=True):
         end.record(stream)
         torch.cuda.synchronize()
     barrier(dist, local)
+    del flush
     elapsed = start.elapsed_time(end) / 1e3
     value, slowest = aggregate(K, elapsed, world, dist, local)
     # every timed step did the workload's work: running canvas, one position committed
@@ -502,7 +505,8 @@ def run_ours(args, rank, world, local):
         "config": {
             "workload": lk["workload"],
             "B": B, "L": L, "V": V, "logits_dtype": lk["name"], "masked": 128, "temperature": TEMPERATURE,
-            "l2": f"10 rotating {lk['bytes'] >> 20} MiB logit buffers ({10 * lk['bytes'] / 2**30:.3g} GiB > 126 MB L2)",
+            "l2": f"10 rotating {lk['bytes'] >> 20} MiB logit buffers ({10 * lk['bytes'] / 2**30:.3g} GiB > 126 MB L2), "
+                  "and a 1 GiB write right before the timed region",
             "launch": f"CUDA graph of {m['N']} steps replayed {m['R']} times (canvas states restored before "
                       "each replay, in the timed region from the second on) "
                       f"after {m['warm_steps']} warm-up steps (at least {WARM_SECONDS} s); row-statistics "

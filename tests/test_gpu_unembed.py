@@ -117,15 +117,16 @@ def test_unembed_equals_written_logits_through_streaming_path():
     assert np.array_equal(a["tokens"], b["tokens"])
 
 
-def test_unembed_full_size_all_rows():
-    """One canvas of the fused workload at full size, every row against the oracle: h [256, 2048]
-    x W [2048, 262144], all masked, T=0.8.  Two row blocks, each split over 74 CTAs along the
-    vocabulary (the small-batch schedule).  The oracle's logits are the binary64 product of the
-    numpy generator's h and W, formed 64 rows of W at a time (each chunk is also compared with
-    the device's W); its step runs on all 256 rows, and compare_step checks every row and the
-    selection, counting as ties the rows whose argmax or sample lies within the fp32
-    accumulation bound."""
-    B, L, K, V = 1, 256, 2048, 262144
+@pytest.mark.parametrize("B", [1, 4])
+def test_unembed_full_size_all_rows(B):
+    """The fused workload at full size, every row against the oracle: h [B 256, 2048] x W [2048,
+    262144], all masked, T=0.8.  B=1 is the small-batch schedule (two row blocks, each split over
+    74 CTAs along the vocabulary); B=4 is the fused workload as the benchmark runs it.  The
+    oracle's logits are the binary64 product of the numpy generator's h and W, formed 64 rows of
+    W at a time (each chunk is also compared with the device's W); its step runs on all rows,
+    and compare_step checks every row and the selection, counting as ties the rows whose argmax
+    or sample lies within the fp32 accumulation bound."""
+    L, K, V = 256, 2048, 262144
     u = eb_synth.cfg4()
     h = torch.empty((B * L, K), dtype=torch.int16, device="cuda")
     W = torch.empty((K, V), dtype=torch.int16, device="cuda")
@@ -136,6 +137,7 @@ def test_unembed_full_size_all_rows():
     c = eb.Canvas(B, L, V, eb.EB_BF16)
     c.unembed_step(gp, h, W, K, 0, 0.8)
     g = host_state(c)
+    assert (g["status"] == eb.EB_RUNNING).all() and (g["committed"] >= 1).all()
     Wd = W.cpu().numpy().view(np.uint16)
     del W
     x64 = np.zeros((B * L, V))
@@ -153,7 +155,7 @@ def test_unembed_full_size_all_rows():
     ost = oracle.State.fresh(B, L)
     res = oracle.step(x64.reshape(B, L, V), ost, 0, op, temperature=T)
     atie, ytie = _ties(x64, K * 2.0 ** -23 * absx, res.gap.reshape(-1), T)
-    rep = Report(label="fused 1x256x2048x262144, all rows")
+    rep = Report(label=f"fused {B}x256x2048x262144, all rows")
     compare_step(g, res, ost, np.ones(B, bool), rep, ctx="fused full size", atie=atie.reshape(B, L),
                  ytie_extra=ytie.reshape(B, L))
     assert rep.rows == B * L and rep.max_h_err < H_TOL
@@ -161,61 +163,6 @@ def test_unembed_full_size_all_rows():
     # wider than the error the tensor cores actually make, so a fifth of the rows fall in it
     # (39 of 256 at V = 8192 already); every row outside it matched exactly above
     assert rep.row_ties <= (B * L) // 3, rep.line()
-
-
-@pytest.mark.parametrize("B,rows", [
-    (4, [0, 1, 127, 128, 300, 511, 640, 1023]),   # the fused workload as the benchmark runs it
-])
-def test_unembed_full_size_sampled_rows(B, rows):
-    """B canvases x 256 positions, K=2048, V=262144, all masked, T=0.8: device inputs equal
-    the numpy generator's, and sampled rows match the oracle one by one.  B=1 is the
-    small-batch case, where each row block is split over many CTAs along the vocabulary."""
-    L, K, V = 256, 2048, 262144
-    u = eb_synth.cfg4()
-    h = torch.empty((B * L, K), dtype=torch.int16, device="cuda")
-    W = torch.empty((K, V), dtype=torch.int16, device="cuda")
-    synth_dev.unembed_inputs(u.seed, B * L, K, V, u.sigma_w, u.bias, h, W)
-    hb = u.h()[: B * L]
-    assert np.array_equal(h.cpu().numpy().view(np.uint16), hb)
-    gp, op = params_pair(seed=0)
-    c = eb.Canvas(B, L, V, eb.EB_BF16)
-    c.unembed_step(gp, h, W, K, 0, 0.8)
-    g = host_state(c)
-    assert (g["status"] == eb.EB_RUNNING).all() and (g["committed"] >= 1).all()
-    rows = np.array(rows)
-    # binary64 logits of the sampled rows, accumulated over the numpy W in row chunks;
-    # the device W is compared with the numpy W chunk by chunk on the way
-    Wd = W.cpu().numpy().view(np.uint16)
-    x64 = np.zeros((rows.shape[0], V))
-    absx = np.zeros((rows.shape[0], V))
-    hf = oracle.bf16_to_f64(hb[rows])
-    for k0 in range(0, K, 64):
-        kk = np.arange(k0, k0 + 64)
-        Wn = eb_synth.unembed_W_rows(u.seed, kk, V, u.sigma_w, u.bias)
-        assert np.array_equal(Wn, Wd[k0:k0 + 64]), f"generator rows {k0}.."
-        Wf = oracle.bf16_to_f64(Wn)
-        x64 += hf[:, k0:k0 + 64] @ Wf
-        absx += np.abs(hf[:, k0:k0 + 64]) @ np.abs(Wf)
-    T = oracle.temperature(0, 48, op.t_start, op.t_end)
-    E = K * 2.0 ** -23 * absx.max(axis=1)
-    for i, r in enumerate(rows):
-        b, p = divmod(int(r), L)
-        H, A, Y, gap = oracle.row(x64[i], T, True, 0, b, p, 0)
-        assert abs(g["entropy"][b, p] - H) <= H_TOL, (r, g["entropy"][b, p], H)
-        top2 = np.sort(x64[i])[-2:]
-        if top2[1] - top2[0] >= 2 * E[i]:
-            assert g["argmax"][b, p] == A, r
-        if gap >= max(1e-6, 2 * E[i] / T):
-            assert g["sampled"][b, p] == Y, r
-    # selection from the GPU's own entropies: exactly the k lowest (H, p) masked positions
-    for b in range(B):
-        Hb = g["entropy"][b].astype(np.float64)
-        order = np.lexsort((np.arange(L), Hb))
-        before = np.concatenate([[0.0], np.cumsum(Hb[order])[:-1]])
-        if np.min(np.abs(before[1:] - float(np.float32(0.1)))) < 1e-5:
-            continue
-        k = int(np.sum((np.arange(L) == 0) | (before <= float(np.float32(0.1)))))
-        assert sorted(np.nonzero(g["selected"][b])[0].tolist()) == sorted(order[:k].tolist())
 
 
 def test_unembed_rejects_bad_shapes():

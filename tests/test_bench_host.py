@@ -1,9 +1,11 @@
 """CPU checks of the benchmark's host logic: the traffic line is taken from the profile summary
 only while the kernel sources hash the same, the clock summary reads nvidia-smi's CSV rows
-(median SM clock, throttle reasons), and the default run keeps at least three warm-up steps."""
+(median SM clock, throttle reasons), the default run keeps at least three warm-up steps, and the
+parity summary of the bench line counts mismatches and near-ties."""
 import os
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -69,3 +71,35 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h
     src.write_text("int f(int x) { return x + 2; }\n")
     assert bench.kernel_source_hash() != h
+
+
+def test_parity_summary_counts_mismatches_and_near_ties():
+    """The bench line's parity summary: a real sample mismatch, a near-tie mismatch (counted
+    apart), an unmasked row's sample (ignored), an argmax mismatch and the selection test."""
+    import types
+
+    import bench
+    L = 6
+    res = types.SimpleNamespace(
+        H=np.zeros((1, L)), A=np.arange(L)[None, :], Y=np.arange(L)[None, :] + 10,
+        gap=np.array([[1.0, 1e-7, 1.0, 1.0, 1.0, 1.0]]),
+        sum_margin=np.array([0.5]), order_margin=np.array([0.5]))
+    H = np.full((1, L), 2e-6)
+    A = res.A.copy()
+    A[0, 5] = 0
+    Y = res.Y.copy()
+    Y[0, 0] += 1            # masked, clear gap: a mismatch
+    Y[0, 1] += 1            # masked, gap below 1e-6: a near-tie
+    Y[0, 2] += 1            # not masked: no sample is compared
+    before = np.array([[1, 1, 0, 1, 1, 1]], np.uint8)
+    after = np.array([[0, 1, 0, 1, 1, 1]], np.uint8)
+    p = bench.parity_summary(H, A, Y, after, before, res, after.copy())
+    assert p["rows"] == L and abs(p["max_abs_dH"] - 2e-6) < 1e-12
+    assert p["argmax_mismatch"] == 1
+    assert p["sample_mismatch"] == 1 and p["sample_ties"] == 1
+    assert p["selection_equal"] and not p["canvas_tie"]
+    other = after.copy()
+    other[0, 3] = 0
+    res.order_margin = np.array([1e-5])
+    p = bench.parity_summary(H, A, Y, after, before, res, other)
+    assert not p["selection_equal"] and p["canvas_tie"]
